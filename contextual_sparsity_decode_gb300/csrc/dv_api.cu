@@ -1,0 +1,378 @@
+// C ABI of libdv: argument validation, workspace layout and kernel launches.
+// Every entry point checks its arguments on the host before launching
+// anything and never synchronises (except dv_check).
+
+#include <cstdint>
+#include <cstring>
+
+#include "dv_kernels.h"
+
+using namespace dv;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+dv_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return DV_ERR_CUDA;
+}
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int vec_of(dv_dtype dt) { return dt == DV_F32 ? 4 : 8; }
+bool dtype_ok(dv_dtype dt) { return dt == DV_F32 || dt == DV_F16 || dt == DV_BF16; }
+
+// Largest cluster / slice count (<= 8) splitting d into <= 256 chunks per CTA.
+bool row_splits_ok(int d, dv_dtype dt) {
+  const int chunks = d / vec_of(dt);
+  for (int cs = 1; cs <= 8; ++cs)
+    if (chunks % cs == 0 && chunks / cs <= 256) return true;
+  return false;
+}
+
+// Sequential carving of 256-byte aligned regions out of a workspace.  With a
+// null base it only measures.
+struct Carver {
+  char* base;
+  size_t off = sizeof(WsHeader);
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+  size_t size() const { return (off + 255) & ~size_t(255); }
+};
+
+constexpr int kMaxB = 32;
+
+// ---- workspace layouts --------------------------------------------------------
+
+struct PredWs {
+  float* h[2];
+  float* s[2];
+};
+PredWs carve_pred(Carver& c, int B, int n_preds, const int* r, const int* N) {
+  PredWs w{};
+  for (int i = 0; i < n_preds; ++i) {
+    w.h[i] = c.take<float>((size_t)B * r[i]);
+    w.s[i] = c.take<float>((size_t)B * N[i]);
+  }
+  return w;
+}
+
+struct MlpWs {
+  int32_t* U;
+  int32_t* U_count;
+  uint32_t* member;
+};
+MlpWs carve_mlp(Carver& c, int B, int N) {
+  MlpWs w{};
+  w.U = c.take<int32_t>((size_t)N);
+  w.U_count = c.take<int32_t>(4);
+  w.member = c.take<uint32_t>((size_t)B * ((N + 31) / 32));
+  return w;
+}
+
+struct AttnWs {
+  int32_t* U;
+  int32_t* U_count;
+  uint32_t* member;
+  int32_t* slot_of;
+  float* q;
+  float* part;
+  int* ticket;
+  float* H;
+};
+AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
+  AttnWs w{};
+  const int capU = B == 1 ? cap : h;
+  const int n_chunks = (n_max + kAttnChunk - 1) / kAttnChunk;
+  w.U = c.take<int32_t>((size_t)h);
+  w.U_count = c.take<int32_t>(4);
+  w.member = c.take<uint32_t>((size_t)B * ((h + 31) / 32));
+  w.slot_of = c.take<int32_t>((size_t)h);
+  w.q = c.take<float>((size_t)B * capU * d_h);
+  w.part = c.take<float>((size_t)B * cap * n_chunks * (d_h + 2));
+  w.ticket = c.take<int>((size_t)B * cap);
+  w.H = c.take<float>((size_t)B * capU * d_h);
+  return w;
+}
+
+// ---- validation ---------------------------------------------------------------------
+
+dv_status check_pred(const void* y, int B, int d, dv_dtype dt, const dv_predictor* preds,
+                     int n_preds) {
+  if (!dtype_ok(dt)) return DV_ERR_DTYPE;
+  if (!y || !aligned16(y) || !preds || n_preds < 1 || n_preds > 2) return DV_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxB || d < 1 || d > 16384 || d % vec_of(dt)) return DV_ERR_INVALID_ARG;
+  for (int i = 0; i < n_preds; ++i) {
+    const dv_predictor& p = preds[i];
+    if (!p.P1t || !p.P2t || !p.idx || !p.count) return DV_ERR_INVALID_ARG;
+    if (!aligned16(p.P1t) || !aligned16(p.P2t) || !aligned4(p.idx) || !aligned4(p.count))
+      return DV_ERR_INVALID_ARG;
+    if (p.scores && !aligned4(p.scores)) return DV_ERR_INVALID_ARG;
+    if (p.r < 1 || p.r > 4096 || p.r % vec_of(dt)) return DV_ERR_INVALID_ARG;
+    if (p.N < 1 || p.N > kSelectMaxN || p.cap < 1) return DV_ERR_INVALID_ARG;
+    if (p.mode != DV_TOPK && p.mode != DV_THRESHOLD) return DV_ERR_INVALID_ARG;
+    if (p.mode == DV_TOPK && (p.k < 0 || p.k > p.N || p.k > p.cap)) return DV_ERR_INVALID_ARG;
+  }
+  return DV_OK;
+}
+
+bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
+  return ws && aligned16(ws) && ws_bytes >= need;
+}
+
+}  // namespace
+
+namespace {
+dv_status check_attn(const void* y, int B, int d, int h, int d_h, const void* Wqkv,
+                     const void* Wo, const dv_kv* kv, const int32_t* pos,
+                     const int32_t* head_idx, int cap, const int32_t* head_count, dv_dtype dt,
+                     bool need_y_wo) {
+  if (!dtype_ok(dt)) return DV_ERR_DTYPE;
+  if (!Wqkv || !kv || !pos || !head_idx || !head_count) return DV_ERR_INVALID_ARG;
+  if (need_y_wo && (!y || !Wo || !aligned16(y) || !aligned16(Wo))) return DV_ERR_INVALID_ARG;
+  if (!kv->K || !kv->V || !kv->X || !kv->valid) return DV_ERR_INVALID_ARG;
+  if (!aligned16(Wqkv) || !aligned16(kv->K) || !aligned16(kv->V) || !aligned16(kv->X) ||
+      !aligned16(kv->valid) || !aligned4(pos) || !aligned4(head_idx) || !aligned4(head_count))
+    return DV_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxB || d < 1 || d % vec_of(dt) || h < 1 || h > 1024) return DV_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return DV_ERR_UNSUPPORTED;
+  if (cap < 1 || cap > h) return DV_ERR_INVALID_ARG;
+  if (kv->n_max < 16 || kv->n_max > 65536 || kv->n_max % 16) return DV_ERR_INVALID_ARG;
+  if (!row_splits_ok(d, dt)) return DV_ERR_UNSUPPORTED;
+  return DV_OK;
+}
+
+AttnLaunch make_attn(const void* y, int B, int d, int h, int d_h, const void* Wqkv, const void* Wo,
+                     const dv_kv* kv, const int32_t* pos, const int32_t* head_idx, int cap,
+                     const int32_t* head_count, float scale, float* out, int accumulate,
+                     const AttnWs& w) {
+  AttnLaunch L{};
+  L.y = y; L.B = B; L.d = d; L.h = h; L.d_h = d_h; L.Wqkv = Wqkv; L.Wo = Wo;
+  L.K = kv->K; L.V = kv->V; L.X = kv->X; L.valid = kv->valid; L.n_max = kv->n_max;
+  L.pos = pos; L.head_idx = head_idx; L.cap = cap; L.head_count = head_count;
+  L.scale = scale; L.out = out; L.accumulate = accumulate ? 1 : 0;
+  L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.slot_of = w.slot_of;
+  L.q = w.q; L.part = w.part; L.ticket = w.ticket; L.H = w.H;
+  return L;
+}
+}  // namespace
+
+extern "C" {
+
+const char* dv_status_str(dv_status s) {
+  switch (s) {
+    case DV_OK: return "ok";
+    case DV_ERR_INVALID_ARG: return "invalid argument";
+    case DV_ERR_DTYPE: return "unsupported data type";
+    case DV_ERR_WORKSPACE: return "workspace missing or too small";
+    case DV_ERR_CUDA: return "CUDA error";
+    case DV_ERR_INDEX_RANGE: return "index out of range (skipped on the device)";
+    case DV_ERR_TIMEOUT: return "device wait timed out";
+    case DV_ERR_UNSUPPORTED: return "shape not supported";
+    case DV_ERR_CAPACITY: return "list longer than its capacity (truncated)";
+    case DV_ERR_POSITION: return "position outside the KV cache";
+  }
+  return "unknown status";
+}
+
+int dv_last_cuda_error(void) { return g_last_cuda_error; }
+
+int dv_version(void) { return 100; }
+
+dv_status dv_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws || ws_bytes < sizeof(WsHeader)) return DV_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+dv_status dv_check(void* ws, cudaStream_t stream, int* info) {
+  if (!ws) return DV_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int hv[2] = {0, 0};
+  e = cudaMemcpy(hv, ws, sizeof(hv), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (info) *info = hv[1];
+  if (hv[0] != 0) {
+    e = cudaMemset(ws, 0, sizeof(hv));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return (dv_status)hv[0];
+}
+
+// ---- predictor ------------------------------------------------------------------------
+
+dv_status dv_predict_workspace_size(int B, int n_preds, int r_max, int N_max, size_t* bytes) {
+  if (!bytes || B < 1 || B > kMaxB || n_preds < 1 || n_preds > 2 || r_max < 1 || N_max < 1)
+    return DV_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  const int r[2] = {r_max, r_max}, N[2] = {N_max, N_max};
+  carve_pred(c, B, n_preds, r, N);
+  *bytes = c.size();
+  return DV_OK;
+}
+
+dv_status dv_predict(const void* y, int B, int d, dv_dtype dt, const dv_predictor* preds,
+                     int n_preds, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dv_status st = check_pred(y, B, d, dt, preds, n_preds);
+  if (st != DV_OK) return st;
+  int r[2] = {0, 0}, N[2] = {0, 0};
+  for (int i = 0; i < n_preds; ++i) { r[i] = preds[i].r; N[i] = preds[i].N; }
+  Carver meas(nullptr);
+  carve_pred(meas, B, n_preds, r, N);
+  if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
+  Carver c(ws);
+  PredWs w = carve_pred(c, B, n_preds, r, N);
+  PredLaunch L{};
+  for (int i = 0; i < n_preds; ++i) {
+    const dv_predictor& p = preds[i];
+    L.P1t[i] = p.P1t; L.P2t[i] = p.P2t; L.r[i] = p.r; L.N[i] = p.N;
+    L.mode[i] = (int)p.mode; L.k[i] = p.k; L.t[i] = p.t;
+    L.idx[i] = p.idx; L.cap[i] = p.cap; L.count[i] = p.count;
+    L.h[i] = w.h[i];
+    L.s[i] = p.scores ? p.scores : w.s[i];
+  }
+  cudaError_t e = launch_predict(y, B, d, dt, L, n_preds, static_cast<WsHeader*>(ws), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+dv_status dv_lookahead(const void* y, int B, int d, dv_dtype dt, const dv_predictor* preds,
+                       int n_preds, void* ws, size_t ws_bytes, cudaEvent_t input_ready,
+                       cudaStream_t side, cudaEvent_t done) {
+  dv_status st = check_pred(y, B, d, dt, preds, n_preds);
+  if (st != DV_OK) return st;
+  if (input_ready) {
+    cudaError_t e = cudaStreamWaitEvent(side, input_ready, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  st = dv_predict(y, B, d, dt, preds, n_preds, ws, ws_bytes, side);
+  if (st != DV_OK) return st;
+  if (done) {
+    cudaError_t e = cudaEventRecord(done, side);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return DV_OK;
+}
+
+// ---- sparse MLP -------------------------------------------------------------------------
+
+dv_status dv_sparse_mlp_workspace_size(int B, int d, int N, int cap, size_t* bytes) {
+  if (!bytes || B < 1 || B > kMaxB || d < 1 || N < 1 || cap < 1) return DV_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  carve_mlp(c, B, N);
+  *bytes = c.size();
+  return DV_OK;
+}
+
+dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, const void* W2n,
+                        const int32_t* idx, int cap, const int32_t* count, dv_dtype dt,
+                        float* out, int accumulate, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  if (!dtype_ok(dt)) return DV_ERR_DTYPE;
+  if (!y || !W1n || !W2n || !idx || !count || !out) return DV_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(W1n) || !aligned16(W2n) || !aligned16(out) ||
+      !aligned4(idx) || !aligned4(count))
+    return DV_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxB || d < 1 || d % vec_of(dt) || N < 1 || N > 65536 || cap < 1)
+    return DV_ERR_INVALID_ARG;
+  if (!row_splits_ok(d, dt)) return DV_ERR_UNSUPPORTED;
+  Carver meas(nullptr);
+  carve_mlp(meas, B, N);
+  if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
+  Carver c(ws);
+  MlpWs w = carve_mlp(c, B, N);
+  MlpLaunch L{};
+  L.y = y; L.B = B; L.d = d; L.N = N; L.W1n = W1n; L.W2n = W2n;
+  L.idx = idx; L.cap = cap; L.count = count; L.out = out; L.accumulate = accumulate ? 1 : 0;
+  L.U = w.U; L.U_count = w.U_count; L.member = w.member;
+  cudaError_t e = launch_sparse_mlp(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+// ---- attention ----------------------------------------------------------------------------
+
+dv_status dv_sparse_attn_workspace_size(int B, int d, int h, int d_h, int cap, int n_max,
+                                        size_t* bytes) {
+  if (!bytes || B < 1 || B > kMaxB || d < 1 || h < 1 || d_h < 1 || cap < 1 || n_max < 1)
+    return DV_ERR_INVALID_ARG;
+  Carver c(nullptr);
+  carve_attn(c, B, h, d_h, cap, n_max);
+  *bytes = c.size();
+  return DV_OK;
+}
+
+
+dv_status dv_sparse_attn(const void* y, int B, int d, int h, int d_h, const void* Wqkv,
+                         const void* Wo, const dv_kv* kv, const int32_t* pos,
+                         const int32_t* head_idx, int cap, const int32_t* head_count, float scale,
+                         dv_dtype dt, float* out, int accumulate, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+  dv_status st = check_attn(y, B, d, h, d_h, Wqkv, Wo, kv, pos, head_idx, cap, head_count, dt, true);
+  if (st != DV_OK) return st;
+  if (!out || !aligned16(out)) return DV_ERR_INVALID_ARG;
+  Carver meas(nullptr);
+  carve_attn(meas, B, h, d_h, cap, kv->n_max);
+  if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
+  Carver c(ws);
+  AttnWs w = carve_attn(c, B, h, d_h, cap, kv->n_max);
+  AttnLaunch L = make_attn(y, B, d, h, d_h, Wqkv, Wo, kv, pos, head_idx, cap, head_count, scale,
+                           out, accumulate, w);
+  cudaError_t e = launch_sparse_attn(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h, const void* Wqkv,
+                       const int32_t* pos, const int32_t* head_idx, int cap,
+                       const int32_t* head_count, dv_dtype dt, void* ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  dv_status st = check_attn(nullptr, B, d, h, d_h, Wqkv, nullptr, kv, pos, head_idx, cap, head_count,
+                            dt, false);
+  if (st != DV_OK) return st;
+  Carver meas(nullptr);
+  carve_attn(meas, B, h, d_h, cap, kv->n_max);
+  if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
+  Carver c(ws);
+  AttnWs w = carve_attn(c, B, h, d_h, cap, kv->n_max);
+  AttnLaunch L = make_attn(nullptr, B, d, h, d_h, Wqkv, nullptr, kv, pos, head_idx, cap, head_count,
+                           1.f, nullptr, 0, w);
+  cudaError_t e = launch_kv_repair(L, dt, static_cast<WsHeader*>(ws), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+// ---- helpers ----------------------------------------------------------------------------------
+
+dv_status dv_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtype dt,
+                       cudaStream_t stream) {
+  if (!dtype_ok(dt)) return DV_ERR_DTYPE;
+  if (!x || !y || B < 1 || d < 1 || !(eps >= 0.f)) return DV_ERR_INVALID_ARG;
+  cudaError_t e = launch_layernorm(x, B, d, eps, y, dt, stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+dv_status dv_positions_advance(int32_t* pos, int B, int lo, int hi, cudaStream_t stream) {
+  if (!pos || B < 1 || lo < 0 || hi <= lo) return DV_ERR_INVALID_ARG;
+  cudaError_t e = launch_positions_advance(pos, B, lo, hi, stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+// Device helpers shared by the kernels of libdv (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dv.h"
+
+namespace dv {
+
+constexpr int kWarp = 32;
+
+// Workspace header: error word (first code wins) and the offending value.
+struct WsHeader {
+  int err;
+  int info;
+  int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header keeps 256-byte alignment");
+
+__device__ __forceinline__ void set_error(WsHeader* hdr, int code, int info) {
+  if (atomicCAS(&hdr->err, 0, code) == 0) hdr->info = info;
+}
+
+// ---- storage types --------------------------------------------------------
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__half> {
+  static constexpr int kVec = 8;
+  static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+  static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// 16-byte streaming load of weights: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// 16-byte load through L1 (activations / vectors re-read by several warps).
+__device__ __forceinline__ uint4 ld_cached(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Unpack a 16-byte vector of T into floats (kVec values).
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& v, float* f);
+
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4& v, float* f) {
+  f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ __forceinline__ void unpack<__half>(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+    float2 p = __half22float2(h2);
+    f[2 * i] = p.x; f[2 * i + 1] = p.y;
+  }
+}
+template <>
+__device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // bf16 -> fp32 is exact: the bf16 bits are the high half of the float.
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Inclusive prefix sum over a block of NT threads (NT multiple of 32, <= 1024).
+// `tmp` holds >= 32 ints of shared memory.  Returns the inclusive sum of
+// thread's value; *total receives the block total.
+template <int NT>
+__device__ __forceinline__ int block_inclusive_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) tmp[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int w = (lane < NT / 32) ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    tmp[lane] = w;  // inclusive warp-total prefix
+  }
+  __syncthreads();
+  if (wid > 0) v += tmp[wid - 1];
+  *total = tmp[NT / 32 - 1];
+  __syncthreads();
+  return v;
+}
+
+// L2 prefetch of a contiguous byte range (address 16-byte aligned, size a
+// multiple of 16): starts the HBM read without staging it anywhere.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Thread-block-cluster barrier, split into arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Read a float from CTA `rank`'s shared memory at the address of `local`.
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t saddr = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(saddr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void atomic_add_f32x4(float* dst, float a, float b, float c, float d) {
+  atomicAdd(reinterpret_cast<float4*>(dst), make_float4(a, b, c, d));
+}
+
+// Membership test in a per-row bitmap of `words` 32-bit words.
+__device__ __forceinline__ bool bit_test(const uint32_t* bm, int i) {
+  return (bm[i >> 5] >> (i & 31)) & 1u;
+}
+
+}  // namespace dv

@@ -1,0 +1,89 @@
+// Host-side launchers of libdv's kernels (one translation unit each).
+// Shapes have been validated by the C-ABI layer before any launcher runs.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "dv_common.cuh"
+
+namespace dv {
+
+// ---- predictor (k_predict.cu) ----------------------------------------------
+
+// Largest unit count a selection CTA stages in shared memory (208 KB).
+constexpr int kSelectMaxN = 53248;
+
+struct PredLaunch {
+  const void* P1t[2];
+  const void* P2t[2];
+  int r[2], N[2];
+  int mode[2], k[2];
+  float t[2];
+  int32_t* idx[2];
+  int cap[2];
+  int32_t* count[2];
+  float* h[2];       // [B][r] fp32 scratch
+  float* s[2];       // [B][N] fp32 scores (caller buffer or scratch)
+};
+
+cudaError_t launch_predict(const void* y, int B, int d, dv_dtype dt,
+                           const PredLaunch& p, int n_preds, WsHeader* hdr,
+                           cudaStream_t stream);
+
+// ---- sparse MLP (k_mlp.cu) ---------------------------------------------------
+
+struct MlpLaunch {
+  const void* y; int B, d, N;
+  const void* W1n; const void* W2n;
+  const int32_t* idx; int cap; const int32_t* count;
+  float* out; int accumulate;
+  // batch union scratch (B > 1)
+  int32_t* U; int32_t* U_count; uint32_t* member;  // member [B][ceil(N/32)]
+};
+
+cudaError_t launch_sparse_mlp(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
+                              int num_sms, cudaStream_t stream);
+
+// Union of per-row index lists: U ascending, U_count, member bitmaps and
+// (optional) slot_of[unit] = position of the unit in U.
+cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B,
+                         int N, int32_t* U, int32_t* U_count, uint32_t* member,
+                         int32_t* slot_of, WsHeader* hdr, cudaStream_t stream);
+
+// ---- attention (k_attn.cu) ---------------------------------------------------
+
+struct AttnLaunch {
+  const void* y; int B, d, h, d_h;
+  const void* Wqkv; const void* Wo;
+  void* K; void* V; void* X; uint8_t* valid; int n_max;
+  const int32_t* pos;
+  const int32_t* head_idx; int cap; const int32_t* head_count;  // per-row lists
+  float scale;
+  float* out; int accumulate;
+  // scratch
+  int32_t* U; int32_t* U_count; uint32_t* member; int32_t* slot_of;  // union (B > 1)
+  float* q;                   // [B][capU][d_h]
+  float* part;                // [B][cap][n_chunks][d_h + 2]
+  int* ticket;                // [B][cap]
+  float* H;                   // [B][capU][d_h]
+};
+
+// Positions per split-KV chunk of the decode kernel.
+constexpr int kAttnChunk = 64;
+
+cudaError_t launch_sparse_attn(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
+                               int num_sms, cudaStream_t stream);
+cudaError_t launch_kv_repair(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
+                             cudaStream_t stream);
+
+// ---- misc (k_misc.cu) --------------------------------------------------------
+
+cudaError_t launch_layernorm(const float* x, int B, int d, float eps, void* y,
+                             dv_dtype dt, cudaStream_t stream);
+cudaError_t launch_positions_advance(int32_t* pos, int B, int lo, int hi,
+                                     cudaStream_t stream);
+
+}  // namespace dv

@@ -1,0 +1,657 @@
+// Sparsified attention with KV repair (Deja Vu reading notes, "Sparsified
+// Attention": MHA_{S_A}(y) = sum_{i in S_A} H_i(y) W_i^O with
+// H_i(y) = D_i(y)^-1 exp(y W_i^Q (W_i^K)^T X^T) X W_i^V; and "Sparsity operator
+// for Attention": skipped heads keep the token embedding and have their K/V
+// recomputed when selected later).
+//
+// One decode step is three kernels:
+//   attn_qkv     one warp per row of W_i^{Q,K,V} of each selected head (head
+//                rows are contiguous: Wqkv[i][m][t][:]).  The warp streams its
+//                row once and dots it with every vector that needs it: the
+//                current token(s) and, for K/V rows, the stored embeddings
+//                X[j] of positions whose K/V were skipped (fused repair, so a
+//                repair costs no extra weight traffic).
+//   attn_decode  split-KV softmax: one CTA per (row, head, 64-position chunk),
+//                online max/sum per warp, partials combined by the last CTA of
+//                each head (ticket counter, no spin wait).  Also appends X[pos]
+//                and updates the valid flags.
+//   attn_out     out += sum_i H_i W_i^O as a weighted sum of the selected
+//                heads' W^O rows, column-sliced across CTAs, fp32 atomics.
+// The standalone repair (dv_kv_repair, e.g. a dense prefill) uses a tiled
+// CUDA-core GEMM over the missing positions instead.
+
+#include "dv_kernels.h"
+
+namespace dv {
+namespace {
+
+constexpr int kEntCap = 8192;      // vector entries per flush in attn_qkv
+constexpr int kVG = 16;            // vectors dotted per pass over a weight row
+constexpr int kCur = 1 << 30;      // entry flag: the current token (vector = y_b)
+constexpr int kCH = kAttnChunk;
+
+struct AttnArgs {
+  const void* y;
+  const void* Wqkv;
+  const void* Wo;
+  void* K;
+  void* V;
+  void* X;
+  uint8_t* valid;
+  const int32_t* pos;
+  const int32_t* head_idx;
+  const int32_t* head_count;
+  int cap;
+  const int32_t* U;
+  const int32_t* U_count;
+  int capU;
+  const uint32_t* member;   // [B][hwords], nullptr when B == 1
+  int hwords;
+  const int32_t* slot_of;   // head -> union slot, nullptr when B == 1
+  int B, d, h, d_h, n_max, n_chunks;
+  float scale;
+  float* q;
+  float* part;
+  int* ticket;
+  float* H;
+  float* out;
+  WsHeader* hdr;
+};
+
+__device__ __forceinline__ bool member_of(const AttnArgs& a, int b, int i) {
+  return a.member ? bit_test(a.member + (size_t)b * a.hwords, i) : true;
+}
+__device__ __forceinline__ int union_count(const AttnArgs& a) {
+  return max(0, min(*a.U_count, a.capU));
+}
+__device__ __forceinline__ int row_pos(const AttnArgs& a, int b) {
+  const int p = a.pos[b];
+  return (p >= 0 && p < a.n_max) ? p : -1;
+}
+
+// ---------------------------------------------------------------------------
+// attn_qkv
+
+template <typename T>
+__device__ void qkv_dots(const AttnArgs& a, const T* wrow, int m, int t, int i, int u,
+                         const int* ent, int n_ent) {
+  constexpr int V = Elem<T>::kVec;
+  const int lane = threadIdx.x & 31;
+  const int C = a.d / V;
+  const T* y = static_cast<const T*>(a.y);
+  const T* X = static_cast<const T*>(a.X);
+  for (int g0 = 0; g0 < n_ent; g0 += kVG) {
+    const int ng = min(kVG, n_ent - g0);
+    float acc[kVG];
+#pragma unroll
+    for (int e = 0; e < kVG; ++e) acc[e] = 0.f;
+    for (int s0 = 0; s0 < C; s0 += 256) {
+      uint4 wv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = s0 + lane + 32 * k;
+        if (c < C) wv[k] = ld_stream(wrow + (size_t)c * V);
+      }
+#pragma unroll
+      for (int e = 0; e < kVG; ++e) {
+        if (e < ng) {
+          const int en = ent[g0 + e];
+          const int b = (en >> 20) & 1023, j = en & 0xfffff;
+          const T* vec = (en & kCur) ? y + (size_t)b * a.d
+                                     : X + ((size_t)b * a.n_max + j) * a.d;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c = s0 + lane + 32 * k;
+            if (c < C) {
+              float wf[V], xf[V];
+              unpack<T>(wv[k], wf);
+              unpack<T>(ld_cached(vec + (size_t)c * V), xf);
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[e] = fmaf(wf[v], xf[v], acc[e]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kVG; ++e) {
+      if (e < ng) {
+        const float s = warp_sum(acc[e]);
+        if (lane == 0) {
+          const int en = ent[g0 + e];
+          const int b = (en >> 20) & 1023, j = en & 0xfffff;
+          if (m == 0) {
+            a.q[((size_t)b * a.capU + u) * a.d_h + t] = s;
+          } else {
+            T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
+            dst[(((size_t)b * a.h + i) * a.n_max + j) * a.d_h + t] = Elem<T>::from_f(s);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) attn_qkv_kernel(AttnArgs a, int RG) {
+  __shared__ int ent[kEntCap];
+  __shared__ int n_ent;
+  const int tid = threadIdx.x, wid = tid >> 5;
+  const int u = blockIdx.x / RG, rg = blockIdx.x % RG;
+  if (u >= union_count(a)) return;
+  const int i = a.U[u];
+  if (i < 0 || i >= a.h) {
+    if (tid == 0 && rg == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
+    return;
+  }
+  const int m = (rg * 8) / a.d_h;  // uniform over the CTA: 8 rows never straddle Q/K/V
+  const int t = rg * 8 + wid - m * a.d_h;
+  const T* wrow = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + t) * a.d;
+
+  if (tid == 0) n_ent = 0;
+  __syncthreads();
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int p = row_pos(a, b);
+    if (p >= 0 && member_of(a, b, i)) ent[atomicAdd(&n_ent, 1)] = kCur | (b << 20) | p;
+  }
+  __syncthreads();
+  if (m == 0) {
+    qkv_dots<T>(a, wrow, m, t, i, u, ent, n_ent);
+    return;
+  }
+  // K/V rows: append the positions whose K/V were skipped, flushing when full
+  for (int b = 0; b < a.B; ++b) {
+    const int p = row_pos(a, b);
+    if (p < 0 || !member_of(a, b, i)) continue;
+    const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
+    for (int base = 0; base < p; base += 4096) {
+      __syncthreads();
+      if (n_ent + 4096 > kEntCap) {
+        qkv_dots<T>(a, wrow, m, t, i, u, ent, n_ent);
+        __syncthreads();
+        if (tid == 0) n_ent = 0;
+        __syncthreads();
+      }
+      const int j0 = base + tid * 16;
+      if (j0 < p) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(vr + j0);
+        const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int j = j0 + k;
+          if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0)
+            ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  qkv_dots<T>(a, wrow, m, t, i, u, ent, n_ent);
+}
+
+// ---------------------------------------------------------------------------
+// attn_decode
+
+template <typename T> struct KvLoad;
+// E consecutive elements of a K or V row for one lane, as floats.
+template <> struct KvLoad<float> {
+  template <int E> static __device__ __forceinline__ void get(const float* p, float* f) {
+    if constexpr (E == 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+      f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    } else {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(p));
+      f[0] = v.x; f[1] = v.y;
+    }
+  }
+};
+template <typename H16> struct KvLoad16 {
+  template <int E> static __device__ __forceinline__ void get(const H16* p, float* f) {
+    if constexpr (E == 4) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+      uint4 q = make_uint4(v.x, v.y, 0u, 0u);
+      float t[8];
+      unpack<H16>(q, t);
+      f[0] = t[0]; f[1] = t[1]; f[2] = t[2]; f[3] = t[3];
+    } else {
+      const uint32_t v = __ldg(reinterpret_cast<const unsigned int*>(p));
+      uint4 q = make_uint4(v, 0u, 0u, 0u);
+      float t[8];
+      unpack<H16>(q, t);
+      f[0] = t[0]; f[1] = t[1];
+    }
+  }
+};
+template <> struct KvLoad<__half> : KvLoad16<__half> {};
+template <> struct KvLoad<__nv_bfloat16> : KvLoad16<__nv_bfloat16> {};
+
+template <typename T, int DH>
+__global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
+  constexpr int E = DH / 32;
+  const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int p = row_pos(a, b);
+  if (s == a.cap) {  // housekeeping of row b: append X[p], reset the valid column
+    if (c != 0) return;
+    if (p < 0) {
+      if (tid == 0) set_error(a.hdr, DV_ERR_POSITION, a.pos[b]);
+      return;
+    }
+    constexpr int V = Elem<T>::kVec;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.y) + (size_t)b * a.d);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + ((size_t)b * a.n_max + p) * a.d);
+    for (int k = tid; k < a.d / V; k += blockDim.x) dst[k] = src[k];
+    for (int i = tid; i < a.h; i += blockDim.x) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
+    __syncthreads();
+    const int cnt = max(0, min(a.head_count[b], a.cap));
+    for (int e = tid; e < cnt; e += blockDim.x) {
+      const int i = a.head_idx[(size_t)b * a.cap + e];
+      if (i >= 0 && i < a.h) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 1;
+    }
+    return;
+  }
+  const int cnt = max(0, min(a.head_count[b], a.cap));
+  if (s >= cnt || p < 0) return;
+  const int i = a.head_idx[(size_t)b * a.cap + s];
+  if (i < 0 || i >= a.h) {
+    if (tid == 0 && c == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
+    return;
+  }
+  const int u = a.slot_of ? a.slot_of[i] : s;
+  const int n_pos = p + 1;
+  const int nch = (n_pos + kCH - 1) / kCH;
+  if (c >= nch) return;
+  const int j0 = c * kCH, j1 = min(n_pos, j0 + kCH);
+
+  __shared__ float sm[4], sl[4];
+  __shared__ float sacc[4][DH];
+  __shared__ int is_last;
+
+  float qr[E];
+  const float* qg = a.q + ((size_t)b * a.capU + u) * DH + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) qr[e] = qg[e] * a.scale;
+
+  const T* Kr = static_cast<const T*>(a.K) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
+  const T* Vr = static_cast<const T*>(a.V) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
+  float mw = -INFINITY, lw = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int j = j0 + wid; j < j1; j += 4) {
+    float kf[E], vf[E];
+    KvLoad<T>::template get<E>(Kr + (size_t)j * DH, kf);
+    KvLoad<T>::template get<E>(Vr + (size_t)j * DH, vf);
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
+    const float logit = warp_sum(dot);
+    const float mn = fmaxf(mw, logit);
+    const float corr = expf(mw - mn);
+    const float pj = expf(logit - mn);
+    lw = lw * corr + pj;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, vf[e], acc[e] * corr);
+    mw = mn;
+  }
+  if (lane == 0) { sm[wid] = mw; sl[wid] = lw; }
+#pragma unroll
+  for (int e = 0; e < E; ++e) sacc[wid][lane * E + e] = acc[e];
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) M = fmaxf(M, sm[w]);
+  float* prt = a.part + (((size_t)b * a.cap + s) * a.n_chunks + c) * (DH + 2);
+  for (int t = tid; t < DH; t += blockDim.x) {
+    float A = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      if (sm[w] != -INFINITY) A += sacc[w][t] * expf(sm[w] - M);
+    prt[2 + t] = A;
+  }
+  if (tid == 0) {
+    float L = 0.f;
+    for (int w = 0; w < 4; ++w)
+      if (sm[w] != -INFINITY) L += sl[w] * expf(sm[w] - M);
+    prt[0] = M;
+    prt[1] = L;
+  }
+  // every position before p of a selected head is now present (repaired above)
+  uint8_t* vrow = a.valid + ((size_t)b * a.h + i) * a.n_max;
+  for (int j = j0 + tid; j < min(j1, p); j += blockDim.x) vrow[j] = 1;
+
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int old = atomicAdd(&a.ticket[(size_t)b * a.cap + s], 1);
+    is_last = (old == nch - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const float* pb = a.part + ((size_t)b * a.cap + s) * a.n_chunks * (DH + 2);
+  float Mg = -INFINITY;
+  for (int k = 0; k < nch; ++k) Mg = fmaxf(Mg, __ldcg(pb + (size_t)k * (DH + 2)));
+  float den = 0.f;
+  for (int k = 0; k < nch; ++k) {
+    const float* pk = pb + (size_t)k * (DH + 2);
+    den += __ldcg(pk + 1) * expf(__ldcg(pk) - Mg);
+  }
+  for (int t = tid; t < DH; t += blockDim.x) {
+    float num = 0.f;
+    for (int k = 0; k < nch; ++k) {
+      const float* pk = pb + (size_t)k * (DH + 2);
+      num += __ldcg(pk + 2 + t) * expf(__ldcg(pk) - Mg);
+    }
+    a.H[((size_t)b * a.capU + u) * DH + t] = num / den;
+  }
+  if (tid == 0) a.ticket[(size_t)b * a.cap + s] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// attn_out: out_b += sum_{u, t} H[b][u][t] * Wo[U[u]][t][:]
+
+struct SlicePlan {
+  int CS = 0, CPR = 0;
+};
+SlicePlan plan_slices(int chunks) {
+  SlicePlan best;
+  for (int pass = 0; pass < 2 && best.CS == 0; ++pass)
+    for (int cs = 8; cs >= 1; --cs) {
+      if (chunks % cs) continue;
+      const int cpr = chunks / cs;
+      if (cpr > 256) continue;
+      if (pass == 0 && cpr % 32) continue;
+      best.CS = cs;
+      best.CPR = cpr;
+      break;
+    }
+  return best;
+}
+
+template <typename T, int BT>
+__global__ void __launch_bounds__(256) attn_out_kernel(AttnArgs a, int CS, int CPR, int b0) {
+  constexpr int V = Elem<T>::kVec;
+  const int tid = threadIdx.x;
+  const int slice = blockIdx.x % CS, g = blockIdx.x / CS, G = gridDim.x / CS;
+  const int col0 = slice * CPR * V;
+  const int nb = min(BT, a.B - b0);
+  const int R = union_count(a) * a.d_h;
+  const int rc = (R + G - 1) / G;
+  const int r0 = min(R, g * rc), r1 = min(R, r0 + rc);
+  const int NG = 256 / CPR, cc = tid % CPR, gi = tid / CPR;
+  if (gi >= NG || r0 >= r1) return;
+  const T* Wo = static_cast<const T*>(a.Wo);
+  float acc[BT][V];
+#pragma unroll
+  for (int b = 0; b < BT; ++b)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[b][v] = 0.f;
+  for (int r = r0 + gi; r < r1; r += 4 * NG) {
+    uint4 wv[4];
+    int ii[4], uu[4], tt[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rr = r + k * NG;
+      ii[k] = -1;
+      if (rr < r1) {
+        uu[k] = rr / a.d_h;
+        tt[k] = rr - uu[k] * a.d_h;
+        ii[k] = a.U[uu[k]];
+        if (ii[k] >= 0 && ii[k] < a.h)
+          wv[k] = ld_stream(Wo + ((size_t)ii[k] * a.d_h + tt[k]) * a.d + col0 + (size_t)cc * V);
+        else
+          ii[k] = -1;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (ii[k] < 0) continue;
+      float wf[V];
+      unpack<T>(wv[k], wf);
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        if (b >= nb) break;
+        const int bb = b0 + b;
+        if (!member_of(a, bb, ii[k]) || row_pos(a, bb) < 0) continue;
+        const float coef = a.H[((size_t)bb * a.capU + uu[k]) * a.d_h + tt[k]];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[b][v] = fmaf(coef, wf[v], acc[b][v]);
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    if (b >= nb) break;
+    float* o = a.out + (size_t)(b0 + b) * a.d + col0 + (size_t)cc * V;
+#pragma unroll
+    for (int v = 0; v < V; v += 4) atomic_add_f32x4(o + v, acc[b][v], acc[b][v + 1], acc[b][v + 2], acc[b][v + 3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// standalone KV repair: tiled GEMM over the missing positions of a head
+
+template <typename T>
+__global__ void __launch_bounds__(256) kv_repair_gemm_kernel(AttnArgs a, int n_ct) {
+  constexpr int V = Elem<T>::kVec;
+  constexpr int TP = 64, TC = 64, KT = 32;
+  __shared__ float Xs[KT][TP + 4];
+  __shared__ float Ws[KT][TC + 4];
+  __shared__ int pos_s[TP];
+  __shared__ int tmp[32];
+  const int tid = threadIdx.x;
+  const int pt = blockIdx.x, s = blockIdx.y;
+  const int b = blockIdx.z / n_ct, ct = blockIdx.z % n_ct;
+  const int per_m = a.d_h / TC;
+  const int m = 1 + ct / per_m, t0 = (ct % per_m) * TC;
+  const int cnt = max(0, min(a.head_count[b], a.cap));
+  if (s >= cnt) return;
+  const int i = a.head_idx[(size_t)b * a.cap + s];
+  const int p = row_pos(a, b);
+  if (i < 0 || i >= a.h || p < 0) {
+    if (tid == 0 && pt == 0 && ct == 0) set_error(a.hdr, p < 0 ? DV_ERR_POSITION : DV_ERR_INDEX_RANGE, p < 0 ? a.pos[b] : i);
+    return;
+  }
+  // ranks [pt*TP, pt*TP + TP) of the ascending list of missing positions
+  const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
+  int seen = 0;
+  for (int base = 0; base < p; base += 256 * 16) {
+    const int j0 = base + tid * 16;
+    uint32_t w4[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+    if (j0 < p) {
+      const uint4 v4 = *reinterpret_cast<const uint4*>(vr + j0);
+      w4[0] = v4.x; w4[1] = v4.y; w4[2] = v4.z; w4[3] = v4.w;
+    }
+    int mine = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      mine += (j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0);
+    int total;
+    const int incl = block_inclusive_scan<256>(mine, tmp, &total);
+    int rank = seen + incl - mine;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if ((j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0)) {
+        const int slot = rank - pt * TP;
+        if (slot >= 0 && slot < TP) pos_s[slot] = j0 + k;
+        ++rank;
+      }
+    }
+    seen += total;
+  }
+  const int np = min(TP, seen - pt * TP);
+  __syncthreads();
+  if (np <= 0) return;
+
+  const T* X = static_cast<const T*>(a.X) + (size_t)b * a.n_max * a.d;
+  const T* W = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + t0) * a.d;
+  const int tp = tid / 16, tc = tid % 16;
+  float acc[4][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+  constexpr int CPRow = KT / V;  // 16-byte chunks per row per K step
+  for (int k0 = 0; k0 < a.d; k0 += KT) {
+    for (int e = tid; e < TP * CPRow; e += 256) {
+      const int row = e / CPRow, ch = e % CPRow;
+      float f[V];
+      if (row < np && k0 + ch * V < a.d) {
+        unpack<T>(ld_cached(X + (size_t)pos_s[row] * a.d + k0 + ch * V), f);
+      } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) f[v] = 0.f;
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) Xs[ch * V + v][row] = f[v];
+    }
+    for (int e = tid; e < TC * CPRow; e += 256) {
+      const int row = e / CPRow, ch = e % CPRow;
+      float f[V];
+      if (k0 + ch * V < a.d) {
+        unpack<T>(ld_stream(W + (size_t)row * a.d + k0 + ch * V), f);
+      } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) f[v] = 0.f;
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) Ws[ch * V + v][row] = f[v];
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < KT; ++kk) {
+      const float4 xa = *reinterpret_cast<const float4*>(&Xs[kk][tp * 4]);
+      const float4 wb = *reinterpret_cast<const float4*>(&Ws[kk][tc * 4]);
+      const float xv[4] = {xa.x, xa.y, xa.z, xa.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(xv[x], wv[y], acc[x][y]);
+    }
+    __syncthreads();
+  }
+  T* dst = static_cast<T*>(m == 1 ? a.K : a.V) + ((size_t)b * a.h + i) * a.n_max * a.d_h;
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int row = tp * 4 + x;
+    if (row >= np) continue;
+    T* d = dst + (size_t)pos_s[row] * a.d_h + t0 + tc * 4;
+#pragma unroll
+    for (int y = 0; y < 4; ++y) d[y] = Elem<T>::from_f(acc[x][y]);
+  }
+}
+
+__global__ void mark_valid_kernel(AttnArgs a) {
+  const int s = blockIdx.x, b = blockIdx.y;
+  const int cnt = max(0, min(a.head_count[b], a.cap));
+  if (s >= cnt) return;
+  const int i = a.head_idx[(size_t)b * a.cap + s];
+  const int p = row_pos(a, b);
+  if (i < 0 || i >= a.h || p < 0) return;
+  uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
+  for (int j = threadIdx.x; j < p; j += blockDim.x) vr[j] = 1;
+}
+
+// ---------------------------------------------------------------------------
+
+AttnArgs make_args(const AttnLaunch& L, WsHeader* hdr) {
+  AttnArgs a{};
+  a.y = L.y; a.Wqkv = L.Wqkv; a.Wo = L.Wo;
+  a.K = L.K; a.V = L.V; a.X = L.X; a.valid = L.valid;
+  a.pos = L.pos; a.head_idx = L.head_idx; a.head_count = L.head_count; a.cap = L.cap;
+  a.B = L.B; a.d = L.d; a.h = L.h; a.d_h = L.d_h; a.n_max = L.n_max;
+  a.n_chunks = (L.n_max + kCH - 1) / kCH;
+  a.scale = L.scale;
+  a.q = L.q; a.part = L.part; a.ticket = L.ticket; a.H = L.H;
+  a.out = L.out; a.hdr = hdr;
+  a.hwords = (L.h + 31) / 32;
+  if (L.B == 1) {
+    a.U = L.head_idx; a.U_count = L.head_count; a.capU = L.cap;
+    a.member = nullptr; a.slot_of = nullptr;
+  } else {
+    a.U = L.U; a.U_count = L.U_count; a.capU = L.h;
+    a.member = L.member; a.slot_of = L.slot_of;
+  }
+  return a;
+}
+
+template <typename T>
+cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t stream) {
+  AttnArgs a = make_args(L, hdr);
+  // 1. projections + fused repair
+  const int RG = 3 * a.d_h / 8;
+  attn_qkv_kernel<T><<<a.capU * RG, 256, 0, stream>>>(a, RG);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 2. split-KV softmax, last-CTA combine, cache bookkeeping
+  dim3 g2(a.n_chunks, a.cap + 1, a.B);
+  if (a.d_h == 128) attn_decode_kernel<T, 128><<<g2, 128, 0, stream>>>(a);
+  else attn_decode_kernel<T, 64><<<g2, 128, 0, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 3. output projection
+  if (!L.accumulate) {
+    e = cudaMemsetAsync(L.out, 0, (size_t)L.B * L.d * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+  }
+  const SlicePlan sp = plan_slices(a.d / Elem<T>::kVec);
+  if (sp.CS == 0) return cudaErrorInvalidValue;
+  int G = (2 * num_sms) / sp.CS;
+  const int by_rows = (a.capU * a.d_h + 15) / 16;
+  G = G < by_rows ? G : by_rows;
+  G = G < 1 ? 1 : G;
+  for (int b0 = 0; b0 < a.B;) {
+    const int nb = a.B - b0;
+    const int bt = nb >= 8 ? 8 : (nb >= 4 ? 4 : (nb >= 2 ? 2 : 1));
+    switch (bt) {
+      case 8: attn_out_kernel<T, 8><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
+      case 4: attn_out_kernel<T, 4><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
+      case 2: attn_out_kernel<T, 2><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
+      default: attn_out_kernel<T, 1><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    b0 += bt;
+  }
+  return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t repair_t(const AttnLaunch& L, WsHeader* hdr, cudaStream_t stream) {
+  AttnArgs a = make_args(L, hdr);
+  const int n_ct = 2 * a.d_h / 64;
+  dim3 g((a.n_max + 63) / 64, a.cap, a.B * n_ct);
+  kv_repair_gemm_kernel<T><<<g, 256, 0, stream>>>(a, n_ct);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mark_valid_kernel<<<dim3(a.cap, a.B), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(const AttnLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms,
+                               cudaStream_t stream) {
+  if (L.B > 1) {
+    cudaError_t e = launch_union(L.head_idx, L.cap, L.head_count, L.B, L.h, L.U, L.U_count,
+                                 L.member, L.slot_of, hdr, stream);
+    if (e != cudaSuccess) return e;
+  }
+  switch (dt) {
+    case DV_F32: return attn_t<float>(L, hdr, num_sms, stream);
+    case DV_F16: return attn_t<__half>(L, hdr, num_sms, stream);
+    case DV_BF16: return attn_t<__nv_bfloat16>(L, hdr, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_kv_repair(const AttnLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
+  switch (dt) {
+    case DV_F32: return repair_t<float>(L, hdr, stream);
+    case DV_F16: return repair_t<__half>(L, hdr, stream);
+    case DV_BF16: return repair_t<__nv_bfloat16>(L, hdr, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dv

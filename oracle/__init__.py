@@ -53,6 +53,7 @@ from .core import (  # noqa: F401
     dense_mlp_zeroed,
     KVCache,
     kv_append,
+    kv_prefill,
     kv_repair,
     head_output,
     sparse_attn,

@@ -184,19 +184,30 @@ def kv_append(cache: KVCache, y: np.ndarray, Wqkv: np.ndarray, n: int,
         cache.valid[i, n] = True
 
 
+def kv_prefill(cache: KVCache, Wqkv: np.ndarray, n: int) -> None:
+    """A dense prompt of n positions: K/V of every head at positions < n from
+    the stored X (all rows of a head in one product), valid = 1.  Equal to
+    kv_append at every prompt position up to float64 summation order; used
+    to set up timing samples, not by the pins."""
+    for i in range(Wqkv.shape[0]):
+        cache.K[i, :n] = round_to(cache.X[:n] @ Wqkv[i, 1].T, cache.dtype)
+        cache.V[i, :n] = round_to(cache.X[:n] @ Wqkv[i, 2].T, cache.dtype)
+    cache.valid[:, :n] = True
+
+
 def kv_repair(cache: KVCache, Wqkv: np.ndarray, n: int,
               S_A: Sequence[int]) -> int:
     """KV repair: for every selected head and every earlier position j < n
     whose K/V were skipped, reload the stored embedding X[j] and recompute
-    K[i][j] = X[j] W_i^K, V[i][j] = X[j] W_i^V.  Returns the rows repaired."""
+    K[i][j] = X[j] W_i^K, V[i][j] = X[j] W_i^V with the same product as the
+    append step.  Returns the rows repaired."""
     fixed = 0
     for i in S_A:
-        for j in range(n):
-            if not cache.valid[i, j]:
-                cache.K[i, j] = round_to(_proj(Wqkv, i, 1, cache.X[j]), cache.dtype)
-                cache.V[i, j] = round_to(_proj(Wqkv, i, 2, cache.X[j]), cache.dtype)
-                cache.valid[i, j] = True
-                fixed += 1
+        for j in np.flatnonzero(~cache.valid[i, :n]):
+            cache.K[i, j] = round_to(_proj(Wqkv, i, 1, cache.X[j]), cache.dtype)
+            cache.V[i, j] = round_to(_proj(Wqkv, i, 2, cache.X[j]), cache.dtype)
+            cache.valid[i, j] = True
+            fixed += 1
     return fixed
 
 
@@ -276,26 +287,32 @@ def lookahead(y_l: np.ndarray, W_next: dict, k_heads: int, k_neurons: int):
 
 def decode_stack(r: np.ndarray, layers: List[dict], caches: List[KVCache],
                  n: int, c: float, dtype: str, k_heads: int, k_neurons: int,
-                 force_sets=None):
+                 force_sets=None, trace: Optional[list] = None):
     """One decoded token through the stack at position n.
 
     Layer 0 predicts its own sets from its own attention input; every later
     layer l+1 uses the sets predicted from layer l's attention input.
     ``force_sets`` (list of (S_A, S_M) per layer) replaces the predictions.
-    Returns (r_out, sets) with sets[l] = (S_A, S_M) used by layer l.
+    If ``trace`` is a list, the input each layer's sets were predicted from
+    is appended to it.  Returns (r_out, sets) with sets[l] = (S_A, S_M) used
+    by layer l.
     """
     sets = []
     pending = None
+    src = None
     for l, W in enumerate(layers):
         if force_sets is not None:
             S_A, S_M = force_sets[l]
         elif pending is None:
-            y0 = round_to(layernorm(r), dtype)
-            S_A, S_M = lookahead(y0, W, k_heads, k_neurons)
+            src = round_to(layernorm(r), dtype)
+            S_A, S_M = lookahead(src, W, k_heads, k_neurons)
         else:
             S_A, S_M = pending
+        if trace is not None:
+            trace.append(src)
         sets.append((np.asarray(S_A), np.asarray(S_M)))
         r, y_a = decode_layer(r, W, caches[l], n, S_A, S_M, c, dtype)
         if l + 1 < len(layers) and force_sets is None:
             pending = lookahead(y_a, layers[l + 1], k_heads, k_neurons)
+            src = y_a
     return r, sets

@@ -632,3 +632,16 @@ def test_planted_mistake_is_caught(monkeypatch, name, mutant, pins):
     for pin in pins:
         with pytest.raises(AssertionError):
             pin()
+
+
+def test_kv_prefill_matches_append():
+    Wqkv, Wo, X = _attn_case(33, n=7)
+    h, _, d_h, d = Wqkv.shape
+    a = core.KVCache.empty(h, 8, d_h, d, "f64")
+    b = core.KVCache.empty(h, 8, d_h, d, "f64")
+    for j in range(7):
+        core.kv_append(a, X[j], Wqkv, j, range(h))
+    b.X[:7] = X[:7]
+    core.kv_prefill(b, Wqkv, 7)
+    assert np.array_equal(a.valid, b.valid)
+    assert np.allclose(a.K, b.K, rtol=1e-13, atol=1e-13) and np.allclose(a.V, b.V, rtol=1e-13, atol=1e-13)

@@ -1,0 +1,164 @@
+"""GPU parity of dv_sparse_attn and dv_kv_repair with the float64 oracle.
+
+Each case prefills a prompt (dv_kv_repair with every head selected), then
+decodes several steps with random head sets, so heads skipped at earlier
+steps are repaired later.  Checked after every step:
+  * the output against the oracle (relative L2 1e-3 fp16/bf16, 1e-5 fp32);
+  * X[pos] == y exactly; the selected heads' K/V rows at every position
+    <= pos within one unit in the last place of the exact float64 product;
+  * the valid flags (selected heads: all positions <= pos; others: 0 at pos).
+The oracle keeps its own cache and repairs lazily from X, so its values do
+not depend on the kernel's bookkeeping.
+"""
+
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from contextual_sparsity_decode_gb300 import binding as dv
+from dvtest import TORCH, assert_rel_l2, f64, within_ulp
+from synth import draw
+
+pytestmark = pytest.mark.gpu
+
+#   name                 B  d     h   d_h  dtype   prompt         n_max steps k      scale   w_std
+CASES = [
+    ("tiny_f16",         1, 64,   4,  64,  "f16",  [5],           32,   6,    2,     "isq",  None),
+    ("ragged_bf16",      1, 128,  6,  64,  "bf16", [37],          64,   5,    3,     "one",  None),
+    ("f32_dh128",        1, 256,  4,  128, "f32",  [20],          48,   4,    2,     "isq",  None),
+    ("dh128_f16_gaps",   1, 512,  8,  128, "f16",  [3],           64,   30,   1,     "isq",  None),
+    ("opt1.3b_f16",      1, 2048, 32, 64,  "f16",  [512],         528,  3,    7,     "isq",  0.02),
+    ("opt13b_f16",       1, 5120, 40, 128, "f16",  [1024],        1040, 2,    8,     "isq",  0.02),
+    ("batch3_f16",       3, 512,  8,  64,  "f16",  [30, 45, 12],  64,   4,    3,     "isq",  None),
+    ("batch8_bf16",      8, 1024, 16, 128, "bf16", [100] * 8,     128,  3,    4,     "isq",  None),
+    ("all_heads_f16",    1, 256,  8,  64,  "f16",  [17],          32,   3,    8,     "isq",  None),
+    ("random_sizes_f16", 2, 256,  8,  64,  "f16",  [9, 4],        48,   8,    "rnd", "isq",  None),
+]
+
+
+def _layer(name, d, h, d_h, dtype, w_std):
+    s = w_std if w_std is not None else d ** -0.5
+    Wqkv = draw((h, 3, d_h, d), s, 301, name + "/Wqkv", dtype)
+    Wo = draw((h, d_h, d), s, 301, name + "/Wo", dtype)
+    return Wqkv, Wo
+
+
+def _subset(g, h, k):
+    if k == "rnd":
+        k = int(torch.randint(0, h + 1, (1,), generator=g))
+    return torch.sort(torch.randperm(h, generator=g)[:k]).values.to(torch.int32)
+
+
+def _check_cache(kv, caches, Wqkv64, pos, sets, dtype, y64):
+    K, V = f64(kv.K), f64(kv.V)
+    X, valid = f64(kv.X), kv.valid.cpu().numpy()
+    for b, S in enumerate(sets):
+        p = pos[b]
+        assert np.array_equal(X[b, p], y64[b]), "X[pos] must be the token input"
+        for i in range(Wqkv64.shape[0]):
+            assert valid[b, i, p] == (1 if i in S else 0)
+        for i in S:
+            assert np.all(valid[b, i, : p + 1] == 1)
+            Xe = X[b, : p + 1]
+            assert within_ulp(K[b, i, : p + 1], Xe @ Wqkv64[i, 1].T, dtype), f"K row, head {i}"
+            assert within_ulp(V[b, i, : p + 1], Xe @ Wqkv64[i, 2].T, dtype), f"V row, head {i}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_sparse_attn_parity(case):
+    name, B, d, h, d_h, dtype, prompt, n_max, steps, k, scale_kind, w_std = case
+    dev = "cuda"
+    tdt = TORCH[dtype]
+    scale = 1.0 / math.sqrt(d_h) if scale_kind == "isq" else 1.0
+    Wqkv, Wo = _layer(name, d, h, d_h, dtype, w_std)
+    Wqkv64, Wo64 = f64(Wqkv), f64(Wo)
+    Wqkv_d, Wo_d = Wqkv.to(dev), Wo.to(dev)
+    kv = dv.KV.empty(B, h, n_max, d_h, d, tdt, dev)
+    caches = [oracle.KVCache.empty(h, n_max, d_h, d, dtype) for _ in range(B)]
+    # prompt: X rows from the generator; K/V of every head by dv_kv_repair
+    Xp = draw((B, n_max, d), 1.0, 301, name + "/X", dtype)
+    for b in range(B):
+        kv.X[b, : prompt[b]].copy_(Xp[b, : prompt[b]].to(dev))
+        caches[b].X[: prompt[b]] = f64(Xp[b, : prompt[b]])
+    pos = torch.tensor(prompt, dtype=torch.int32, device=dev)
+    all_heads = torch.arange(h, dtype=torch.int32, device=dev).repeat(B, 1)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, h, n_max))
+    dv.dv_kv_repair(kv, Wqkv_d, pos, all_heads, torch.full((B,), h, dtype=torch.int32, device=dev), ws)
+    assert dv.dv_check(ws)[0] == 0
+    K0, valid0 = f64(kv.K), kv.valid.cpu().numpy()
+    for b in range(B):
+        Xe = f64(Xp[b, : prompt[b]])
+        for i in range(h):
+            assert np.all(valid0[b, i, : prompt[b]] == 1) and np.all(valid0[b, i, prompt[b]:] == 0)
+            assert within_ulp(K0[b, i, : prompt[b]], Xe @ Wqkv64[i, 1].T, dtype)
+
+    g = torch.Generator().manual_seed(zlib.crc32(name.encode()))
+    cap = h if k == "rnd" else max(1, k)
+    for step in range(steps):
+        p = [prompt[b] + step for b in range(B)]
+        if max(p) >= n_max:
+            break
+        y = draw((B, d), 1.0, 301, f"{name}/y{step}", dtype)
+        sets = [_subset(g, h, k) for _ in range(B)]
+        idx = torch.full((B, cap), -1, dtype=torch.int32)
+        cnt = torch.zeros(B, dtype=torch.int32)
+        for b, S in enumerate(sets):
+            idx[b, : len(S)] = S
+            cnt[b] = len(S)
+        out = torch.full((B, d), 77.0, device=dev)
+        ws_s = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, cap, n_max))
+        dv.dv_sparse_attn(y.to(dev), Wqkv_d, Wo_d, kv, torch.tensor(p, dtype=torch.int32, device=dev),
+                          idx.to(dev), cnt.to(dev), scale, out, ws_s)
+        st, info = dv.dv_check(ws_s)
+        assert st == 0, (st, info)
+        got = f64(out)
+        y64 = f64(y)
+        for b in range(B):
+            ref = oracle.sparse_attn(y64[b], Wqkv64, Wo64, caches[b], p[b], sets[b].tolist(), scale)
+            if len(sets[b]) == 0:
+                assert np.all(got[b] == 0.0)
+            else:
+                assert_rel_l2(got[b], ref, dtype, f"{name} step {step} row {b}")
+        _check_cache(kv, caches, Wqkv64, p, [S.tolist() for S in sets], dtype, y64)
+
+
+def test_accumulate_into_residual():
+    B, d, h, d_h, n_max = 2, 256, 4, 64, 32
+    Wqkv, Wo = _layer("acc", d, h, d_h, "f16", None)
+    dev = "cuda"
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    y = draw((B, d), 1.0, 302, "acc/y", "f16")
+    base = draw((B, d), 2.0, 302, "acc/base", "f32").to(dev)
+    out = base.clone()
+    idx = torch.tensor([[0, 2], [1, 3]], dtype=torch.int32, device=dev)
+    cnt = torch.tensor([2, 1], dtype=torch.int32, device=dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, 2, n_max))
+    dv.dv_sparse_attn(y.to(dev), Wqkv.to(dev), Wo.to(dev), kv, pos, idx, cnt, 0.125, out, ws,
+                      accumulate=True)
+    assert dv.dv_check(ws)[0] == 0
+    for b, S in enumerate([[0, 2], [1]]):
+        c = oracle.KVCache.empty(h, n_max, d_h, d, "f16")
+        ref = oracle.sparse_attn(f64(y)[b], f64(Wqkv), f64(Wo), c, 0, S, 0.125)
+        assert_rel_l2(f64(out)[b] - f64(base)[b], ref, "f16", "accumulate")
+
+
+def test_position_outside_cache_is_reported():
+    B, d, h, d_h, n_max = 1, 128, 4, 64, 16
+    Wqkv, Wo = _layer("pos", d, h, d_h, "f16", None)
+    dev = "cuda"
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
+    pos = torch.tensor([n_max], dtype=torch.int32, device=dev)   # one past the end
+    idx = torch.tensor([[1]], dtype=torch.int32, device=dev)
+    cnt = torch.tensor([1], dtype=torch.int32, device=dev)
+    out = torch.zeros(B, d, device=dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, 1, n_max))
+    dv.dv_sparse_attn(draw((B, d), 1.0, 303, "y", "f16").to(dev), Wqkv.to(dev), Wo.to(dev), kv, pos,
+                      idx, cnt, 0.125, out, ws)
+    st, info = dv.dv_check(ws)
+    assert st == 9 and info == n_max      # DV_ERR_POSITION; nothing written
+    assert torch.count_nonzero(kv.K) == 0 and torch.count_nonzero(out) == 0

@@ -1,0 +1,133 @@
+"""GPU parity of dv_sparse_mlp with the float64 oracle (given identical
+index lists): relative L2 error <= 1e-3 for fp16 / bf16 and <= 1e-5 for fp32,
+element by element on every output."""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from contextual_sparsity_decode_gb300 import binding as dv
+from dvtest import assert_rel_l2, f64
+from synth import draw, keep_count
+
+pytestmark = pytest.mark.gpu
+
+#        name                     B   d      N      dtype   k
+CASES = [
+    ("tiny_ragged_f16",           1, 64,    100,   "f16",  7),
+    ("d136_f16",                  1, 136,   544,   "f16",  33),
+    ("opt1.3b_f16",               1, 2048,  8192,  "f16",  410),
+    ("opt13b_f16",                1, 5120,  20480, "f16",  1024),
+    ("opt30b_bf16",               1, 7168,  28672, "bf16", 1434),
+    ("opt30b_bf16_half",          1, 7168,  28672, "bf16", 14336),
+    ("opt175b_f16",               1, 12288, 49152, "f16",  2458),
+    ("bf16_small",                1, 512,   2048,  "bf16", 103),
+    ("f32_d1024",                 1, 1024,  4096,  "f32",  205),
+    ("batch3_f16",                3, 1024,  4096,  "f16",  205),
+    ("batch8_f16",                8, 2048,  8192,  "f16",  410),
+    ("batch13_bf16",              13, 1024, 4096,  "bf16", 205),
+    ("all_neurons_f16",           1, 256,   1024,  "f16",  1024),
+    ("one_neuron_f16",            1, 256,   1024,  "f16",  1),
+]
+
+
+def _weights(name, d, N, dtype, wid=201):
+    return (draw((N, d), 0.02, wid, name + "/W1", dtype), draw((N, d), 0.02, wid, name + "/W2", dtype))
+
+
+def _sets(name, B, N, k):
+    g = torch.Generator().manual_seed(zlib.crc32(name.encode()))
+    return [torch.sort(torch.randperm(N, generator=g)[:k]).values.to(torch.int32) for _ in range(B)]
+
+
+def _run(y, W1n, W2n, sets, cap, accumulate=False, base=None):
+    dev = "cuda"
+    B, d = y.shape
+    idx = torch.full((B, cap), -1, dtype=torch.int32)
+    cnt = torch.zeros(B, dtype=torch.int32)
+    for b, s in enumerate(sets):
+        idx[b, : len(s)] = s
+        cnt[b] = len(s)
+    out = (base.clone() if base is not None else torch.full((B, d), 123.0)).to(dev)
+    ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(B, d, W1n.shape[0], cap))
+    dv.dv_sparse_mlp(y.to(dev), W1n.to(dev), W2n.to(dev), idx.to(dev), cnt.to(dev), out, ws,
+                     accumulate=accumulate)
+    st, info = dv.dv_check(ws)
+    return out.cpu().double().numpy(), st, info
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_sparse_mlp_parity(case):
+    name, B, d, N, dtype, k = case
+    W1n, W2n = _weights(name, d, N, dtype)
+    y = draw((B, d), 1.0, 201, name + "/y", dtype)
+    sets = _sets(name, B, N, k)
+    out, st, info = _run(y, W1n, W2n, sets, k)
+    assert st == 0, (st, info)
+    ref = oracle.sparse_mlp_batched(f64(y), f64(W1n), f64(W2n), [s.numpy() for s in sets])
+    for b in range(B):
+        assert_rel_l2(out[b], ref[b], dtype, f"{name} row {b}")
+
+
+def test_fp32_mlp_block_true_preactivation_top5pct():
+    """Single fp32 MLP block, d = 768, 4d = 3072: S_M = the 154 neurons with the
+    largest true pre-activation y . W^1[:, j] (computed by the oracle)."""
+    d, N = 768, 3072
+    k = keep_count(5, N)
+    W1n, W2n = _weights("c1", d, N, "f32", wid=1)
+    y = draw((1, d), 1.0, 1, "c1/y", "f32")
+    pre = f64(W1n) @ f64(y)[0]
+    S = oracle.select_topk(pre, k)
+    out, st, _ = _run(y, W1n, W2n, [torch.from_numpy(S)], k)
+    assert st == 0 and k == 154
+    ref = oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), S)
+    assert_rel_l2(out[0], ref, "f32", "fp32 block")
+
+
+def test_accumulate_adds_to_residual():
+    d, N, k = 1024, 4096, 205
+    W1n, W2n = _weights("acc", d, N, "f16")
+    y = draw((2, d), 1.0, 202, "acc/y", "f16")
+    base = draw((2, d), 3.0, 202, "acc/base", "f32")
+    sets = _sets("acc", 2, N, k)
+    out, st, _ = _run(y, W1n, W2n, sets, k, accumulate=True, base=base)
+    assert st == 0
+    ref = oracle.sparse_mlp_batched(f64(y), f64(W1n), f64(W2n), [s.numpy() for s in sets])
+    for b in range(2):
+        assert_rel_l2(out[b] - f64(base)[b], ref[b], "f16", "accumulate")
+
+
+def test_empty_selection_gives_zero():
+    d, N = 512, 2048
+    W1n, W2n = _weights("empty", d, N, "f16")
+    y = draw((2, d), 1.0, 203, "empty/y", "f16")
+    out, st, _ = _run(y, W1n, W2n, [torch.zeros(0, dtype=torch.int32)] * 2, 16)
+    assert st == 0 and np.all(out == 0.0)
+
+
+def test_out_of_range_index_is_skipped_and_reported():
+    d, N, k = 512, 2048, 20
+    W1n, W2n = _weights("oor", d, N, "f16")
+    y = draw((1, d), 1.0, 204, "oor/y", "f16")
+    S = _sets("oor", 1, N, k)[0].clone()
+    S[-1] = N + 5  # outside [0, N)
+    out, st, info = _run(y, W1n, W2n, [S], k)
+    assert st == 5 and info == N + 5   # DV_ERR_INDEX_RANGE
+    ref = oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), S[:-1].numpy())
+    assert_rel_l2(out[0], ref, "f16", "valid part")
+
+
+def test_batch_rows_use_their_own_sets():
+    """Masked union semantics: each row equals its batch-1 result."""
+    d, N, k = 1024, 4096, 205
+    W1n, W2n = _weights("mask", d, N, "f16")
+    y = draw((4, d), 1.0, 205, "mask/y", "f16")
+    sets = _sets("mask", 4, N, k)
+    out, st, _ = _run(y, W1n, W2n, sets, k)
+    assert st == 0
+    for b in range(4):
+        one, _, _ = _run(y[b:b + 1], W1n, W2n, [sets[b]], k)
+        assert np.allclose(out[b], one[0], rtol=1e-5, atol=1e-6)

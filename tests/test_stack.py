@@ -1,0 +1,92 @@
+"""GPU parity of the decoder stack (look-ahead prediction on a side stream,
+CUDA-graph replay) with the oracle's free-running decode_stack.
+
+Both sides start from the same residual input and prompt embeddings and run
+their own predictors, so index lists are compared with the 1e-5 window rule;
+a list that differs inside the window (a legitimate near-tie flip) makes the
+two trajectories diverge, after which the comparison stops.  Outputs are
+compared by relative L2 (1e-3 for fp16 storage)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from contextual_sparsity_decode_gb300 import binding as dv
+from contextual_sparsity_decode_gb300.stack import SparseDecoder
+from dvtest import assert_rel_l2, check_selection, f64
+from synth import Workload, embeddings, layer_weights, residual_input
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_stack(w: Workload, steps: int, graph_from: int = 1):
+    dev = "cuda"
+    layers_h = [layer_weights(w, l) for l in range(w.layers)]
+    layers_d = [{k: v.to(dev) for k, v in L.items()} for L in layers_h]
+    layers64 = [{k: f64(v) for k, v in L.items()} for L in layers_h]
+    n_max = ((w.n_prompt + steps + 15) // 16) * 16
+    scale = 1.0 / math.sqrt(w.d_h)
+    dec = SparseDecoder(layers_d, 1, n_max, w.k_heads, w.k_neurons, scale)
+    Xp = [embeddings(w, n_max, f"X{l}") for l in range(w.layers)]
+    dec.prefill([x[None].to(dev) for x in Xp], w.n_prompt)
+    caches = []
+    for l in range(w.layers):
+        c = oracle.KVCache.empty(w.h, n_max, w.d_h, w.d, w.dtype)
+        c.X[: w.n_prompt] = f64(Xp[l][: w.n_prompt])
+        caches.append(c)
+    r0 = residual_input(w, 1, "r0")
+    dec.r_stream.copy_(r0.to(dev))
+    r_ref = f64(r0)[0]
+    compared = 0
+    for t in range(steps):
+        n = w.n_prompt + t
+        if t == graph_from:
+            dec.capture(advance=(0, n_max))
+        if t >= graph_from:
+            dec.replay()
+        else:
+            dec.step_ops()
+            dv.dv_positions_advance(dec.pos, 0, n_max)
+        dec.check()
+        trace = []
+        r_ref, sets = oracle.decode_stack(r_ref, layers64, caches, n, scale, w.dtype,
+                                          w.k_heads, w.k_neurons, trace=trace)
+        diverged = False
+        for l in range(w.layers):
+            gA = dec.head_idx[l][0, : int(dec.head_cnt[l][0])].cpu().numpy()
+            gM = dec.neur_idx[l][0, : int(dec.neur_cnt[l][0])].cpu().numpy()
+            _, sA, _ = oracle.predict(trace[l], layers64[l]["PA1t"], layers64[l]["PA2t"], "topk", w.k_heads)
+            _, sM, _ = oracle.predict(trace[l], layers64[l]["PM1t"], layers64[l]["PM2t"], "topk", w.k_neurons)
+            flips = check_selection(gA, sets[l][0], sA[0], "topk", w.k_heads)
+            flips += check_selection(gM, sets[l][1], sM[0], "topk", w.k_neurons)
+            if flips:
+                diverged = True
+                break
+        if diverged:
+            break
+        assert_rel_l2(f64(dec.r_stream)[0], r_ref, w.dtype, f"step {t}")
+        compared += 1
+    return compared
+
+
+def test_tiny_stack_lookahead_graph():
+    w = Workload("tiny_stack", 31, d=256, h=8, d_h=64, N=1024, r=64, dtype="f16", layers=3,
+                 n_prompt=20, n_gen=6, head_pct=25, neuron_pct=5)
+    assert _run_stack(w, steps=6) >= 3
+
+
+def test_bf16_stack_lookahead_graph():
+    w = Workload("bf16_stack", 32, d=512, h=8, d_h=128, N=2048, r=128, dtype="bf16", layers=4,
+                 n_prompt=33, n_gen=5, head_pct=25, neuron_pct=10)
+    assert _run_stack(w, steps=5) >= 2
+
+
+def test_opt13b_width_two_layers():
+    """Two layers of the 40-layer OPT-13B-shaped stack at full width with the
+    1024-position prompt, in the decode configuration the benchmark replays."""
+    w = Workload("opt13b_2l", 3, d=5120, h=40, d_h=128, N=20480, r=1024, dtype="f16", layers=2,
+                 n_prompt=1024, n_gen=3)
+    assert _run_stack(w, steps=3) >= 1
