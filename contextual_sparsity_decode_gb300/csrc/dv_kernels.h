@@ -42,7 +42,17 @@ struct MlpLaunch {
   float* out; int accumulate;
   // batch union scratch (B > 1)
   int32_t* U; int32_t* U_count; uint32_t* member;  // member [B][ceil(N/32)]
+  // tensor-core path: activations split into two storage-type halves,
+  // [32][tc_act_cols(N)] each
+  void* act_hi; void* act_lo;
 };
+
+// Batches of at least this many rows use the tcgen05 path (16-bit types).
+constexpr int kTcMinBatch = 8;
+bool tc_mlp_supported(int B, int d, dv_dtype dt);
+int tc_act_cols(int N);
+cudaError_t launch_sparse_mlp_tc(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
+                                 cudaStream_t stream);
 
 cudaError_t launch_sparse_mlp(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
                               int num_sms, cudaStream_t stream);

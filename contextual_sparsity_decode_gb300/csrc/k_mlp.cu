@@ -359,6 +359,7 @@ cudaError_t launch_sparse_mlp(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, in
                      stream);
     if (e != cudaSuccess) return e;
   }
+  if (L.B > 1 && tc_mlp_supported(L.B, L.d, dt)) return launch_sparse_mlp_tc(L, dt, hdr, stream);
   switch (dt) {
     case DV_F32: return mlp_t<float>(L, hdr, num_sms, stream);
     case DV_F16: return mlp_t<__half>(L, hdr, num_sms, stream);

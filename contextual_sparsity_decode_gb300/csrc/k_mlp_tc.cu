@@ -1,0 +1,386 @@
+// Batched sparsified MLP on the tcgen05 tensor cores.
+//
+// For a batch of B rows the union U of the rows' neuron sets is read once,
+// which turns the gathered weight rows into a real dense contraction
+// (Deja Vu reading notes, "Sparsified MLP", applied to every row with the
+// row's own set as a mask):
+//   up    a[u][b] = ReLU(W^1[:, U[u]] . y_b) * [U[u] in S_b]
+//         M = 128 union neurons per CTA, N = B padded to 16/32, K = d.
+//         A = gathered rows of W1n (TMA gather4, 128-byte swizzle, K-major),
+//         B = y (TMA tile, K-major).  Accumulator in TMEM; the epilogue writes
+//         a split into two storage-type halves hi + lo (a = hi + lo to ~2^-17
+//         relative), so the second product keeps fp32-level accuracy.
+//   down  out[b][c] += sum_u W^2[c, U[u]] a[u][b]
+//         M = 128 output columns per CTA, N = B padded, K = a chunk of U.
+//         A = gathered rows of W2n read as an MN-major operand (a neuron row
+//         is 64 contiguous columns per 128-byte swizzle row), B = a_hi and
+//         a_lo (two MMAs per K step).  Split-K over U with fp32 atomics.
+// One elected thread issues TMA loads into a ring of shared-memory stages,
+// one elected thread issues the MMAs; every wait is bounded and reports
+// DV_ERR_TIMEOUT instead of hanging.
+
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "dv_kernels.h"
+#include "tc_common.cuh"
+
+namespace dv {
+namespace {
+
+constexpr int kTM = 128;                 // tile rows (M)
+constexpr int kKB = 64;                  // K elements per stage (one 128-byte row)
+constexpr int kStages = 4;
+constexpr int kKChunk = 1024;            // union neurons per down-projection CTA
+constexpr long long kWaitLimit = 2000000000LL;  // about one second of cycles
+constexpr uint32_t kTmemCols = 32;
+
+struct UpArgs {
+  const int32_t* U;
+  const int32_t* U_count;
+  int capU;
+  const uint32_t* member;
+  int words, B, d, N, Upad;
+  void* act_hi;
+  void* act_lo;
+  WsHeader* hdr;
+};
+
+struct DownArgs {
+  const int32_t* U;
+  const int32_t* U_count;
+  int capU, B, d, N;
+  float* out;
+  WsHeader* hdr;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <typename T, int BP>
+__global__ void __launch_bounds__(128, 1)
+    mlp_tc_up_kernel(const __grid_constant__ CUtensorMap mapW1, const __grid_constant__ CUtensorMap mapY,
+                     UpArgs a) {
+  constexpr uint32_t kABytes = kTM * 128, kBBytes = BP * 128;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int rows[kTM];
+  __shared__ int flag_err;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cnt = max(0, min(*a.U_count, a.capU));
+  const int u0 = blockIdx.x * kTM;
+  if (u0 >= cnt) return;  // whole CTA, before any barrier or TMEM use
+
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+
+  {
+    int r = a.U[min(u0 + tid, cnt - 1)];
+    if (r < 0 || r >= a.N) {
+      set_error(a.hdr, DV_ERR_INDEX_RANGE, r);
+      r = 0;
+    }
+    rows[tid] = r;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(&done, 1);
+    tc::fence_mbar_init();
+    flag_err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const int nk = a.d / kKB;
+  __shared__ int issued, consumed;
+  if (tid == 0) { issued = 0; consumed = 0; }
+  __syncthreads();
+
+  if (warp == 0 && lane == 0) {  // TMA producer
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, it = kb / kStages;
+      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, kWaitLimit)) {
+        set_error(a.hdr, DV_ERR_TIMEOUT, 1);
+        flag_err = 1;
+        break;
+      }
+      tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+      uint8_t* dA = sA + s * kABytes;
+#pragma unroll 4
+      for (int g = 0; g < kTM / 4; ++g)
+        tc::tma_gather4(dA + g * 512, &mapW1, kb * kKB, rows[4 * g], rows[4 * g + 1], rows[4 * g + 2],
+                        rows[4 * g + 3], &full[s]);
+      tc::tma_load_2d(sB + s * kBBytes, &mapY, kb * kKB, 0, &full[s]);
+      issued = kb + 1;
+    }
+  } else if (warp == 1 && lane == 0) {  // MMA issuer
+    constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+    const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, false, false);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, it = kb / kStages;
+      if (!tc::mbar_wait(&full[s], it & 1, kWaitLimit)) {
+        set_error(a.hdr, DV_ERR_TIMEOUT, 2);
+        flag_err = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t aBase = tc::saddr(sA + s * kABytes), bBase = tc::saddr(sB + s * kBBytes);
+#pragma unroll
+      for (int kk = 0; kk < kKB / 16; ++kk) {
+        const uint64_t ad = tc::smem_desc(aBase + kk * 32, 16, 1024, 2);
+        const uint64_t bd = tc::smem_desc(bBase + kk * 32, 16, 1024, 2);
+        tc::mma_f16(tmem, ad, bd, idesc, (kb | kk) != 0);
+      }
+      tc::mma_commit(&empty[s]);
+      consumed = kb + 1;
+    }
+    tc::mma_commit(&done);  // arrives once every issued MMA has completed
+  }
+  __syncwarp();
+
+  // epilogue: thread = accumulator row (neuron u0 + tid)
+  const bool ok = tc::mbar_wait(&done, 0, kWaitLimit);
+  if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 3);
+  __syncwarp();
+  tc::fence_after_sync();
+  float v[BP];
+#pragma unroll
+  for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
+  tc::tmem_ld_wait();
+  const int u = u0 + tid;
+  const bool live = ok && !flag_err && u < cnt;
+  const int row = rows[tid];
+  T* hi = static_cast<T*>(a.act_hi);
+  T* lo = static_cast<T*>(a.act_lo);
+#pragma unroll
+  for (int b = 0; b < BP; ++b) {
+    float x = fmaxf(v[b], 0.f);
+    if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
+    const T h = Elem<T>::from_f(x);
+    const T l = Elem<T>::from_f(x - Elem<T>::to_f(h));
+    hi[(size_t)b * a.Upad + u] = h;
+    lo[(size_t)b * a.Upad + u] = l;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  // make sure no TMA write into this CTA's shared memory is still in flight
+  if (tid == 0) {
+    for (int kb = consumed; kb < issued; ++kb)
+      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, kWaitLimit)) break;
+  }
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <typename T, int BP>
+__global__ void __launch_bounds__(128, 1)
+    mlp_tc_down_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapHi,
+                       const __grid_constant__ CUtensorMap mapLo, DownArgs a) {
+  constexpr uint32_t kABytes = kKB * 256, kBBytes = BP * 128;  // A: 64 neurons x 128 columns
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int rows[kKChunk];
+  __shared__ int issued, consumed, flag_err;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cnt = max(0, min(*a.U_count, a.capU));
+  const int c0 = blockIdx.x * kTM;
+  const int k0 = blockIdx.y * kKChunk;
+  if (k0 >= cnt) return;
+  const int k1 = min(cnt, k0 + kKChunk);
+  const int nk = (k1 - k0 + kKB - 1) / kKB;
+
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sH = smem + kStages * kABytes;
+  uint8_t* sL = sH + kStages * kBBytes;
+
+  for (int i = tid; i < nk * kKB; i += blockDim.x) {
+    int r = a.U[min(k0 + i, cnt - 1)];
+    if (r < 0 || r >= a.N) {
+      set_error(a.hdr, DV_ERR_INDEX_RANGE, r);
+      r = 0;
+    }
+    rows[i] = r;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(&done, 1);
+    tc::fence_mbar_init();
+    issued = consumed = flag_err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0 && lane == 0) {  // TMA producer
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, it = kb / kStages;
+      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, kWaitLimit)) {
+        set_error(a.hdr, DV_ERR_TIMEOUT, 4);
+        flag_err = 1;
+        break;
+      }
+      tc::mbar_arrive_expect_tx(&full[s], kABytes + 2 * kBBytes);
+      uint8_t* dA = sA + s * kABytes;
+      const int* rr = rows + kb * kKB;
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+#pragma unroll 4
+        for (int g = 0; g < kKB / 4; ++g)
+          tc::tma_gather4(dA + half * (kKB * 128) + g * 512, &mapW2, c0 + half * 64, rr[4 * g], rr[4 * g + 1],
+                          rr[4 * g + 2], rr[4 * g + 3], &full[s]);
+      tc::tma_load_2d(sH + s * kBBytes, &mapHi, k0 + kb * kKB, 0, &full[s]);
+      tc::tma_load_2d(sL + s * kBBytes, &mapLo, k0 + kb * kKB, 0, &full[s]);
+      issued = kb + 1;
+    }
+  } else if (warp == 1 && lane == 0) {  // MMA issuer
+    constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+    const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, /*A MN-major*/ true, false);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, it = kb / kStages;
+      if (!tc::mbar_wait(&full[s], it & 1, kWaitLimit)) {
+        set_error(a.hdr, DV_ERR_TIMEOUT, 5);
+        flag_err = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t aBase = tc::saddr(sA + s * kABytes);
+      const uint32_t hBase = tc::saddr(sH + s * kBBytes), lBase = tc::saddr(sL + s * kBBytes);
+#pragma unroll
+      for (int kk = 0; kk < kKB / 16; ++kk) {
+        // A (MN-major): 16 neuron rows = two 8-row groups (1024 B apart);
+        // the two 64-column halves of the tile are kKB*128 bytes apart
+        const uint64_t ad = tc::smem_desc(aBase + kk * 2048, kKB * 128, 1024, 2);
+        const uint64_t hd = tc::smem_desc(hBase + kk * 32, 16, 1024, 2);
+        const uint64_t ld = tc::smem_desc(lBase + kk * 32, 16, 1024, 2);
+        tc::mma_f16(tmem, ad, hd, idesc, (kb | kk) != 0);
+        tc::mma_f16(tmem, ad, ld, idesc, 1);
+      }
+      tc::mma_commit(&empty[s]);
+      consumed = kb + 1;
+    }
+    tc::mma_commit(&done);
+  }
+  __syncwarp();
+
+  const bool ok = tc::mbar_wait(&done, 0, kWaitLimit);
+  if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 6);
+  __syncwarp();
+  tc::fence_after_sync();
+  float v[BP];
+#pragma unroll
+  for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
+  tc::tmem_ld_wait();
+  if (ok && !flag_err) {
+    const int col = c0 + tid;
+    for (int b = 0; b < a.B; ++b) atomicAdd(a.out + (size_t)b * a.d + col, v[b]);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    for (int kb = consumed; kb < issued; ++kb)
+      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, kWaitLimit)) break;
+  }
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---- host ------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major [rows][cols] 16-bit tensor, box {64 columns, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int BP>
+cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
+  constexpr bool bf16 = !std::is_same<T, __half>::value;
+  const int Upad = tc_act_cols(L.N);
+  CUtensorMap mW1, mW2, mY, mHi, mLo;
+  if (!make_map(&mW1, L.W1n, L.d, L.N, 1, bf16) || !make_map(&mW2, L.W2n, L.d, L.N, 1, bf16) ||
+      !make_map(&mY, L.y, L.d, L.B, BP, bf16) || !make_map(&mHi, L.act_hi, Upad, BP, BP, bf16) ||
+      !make_map(&mLo, L.act_lo, Upad, BP, BP, bf16))
+    return cudaErrorInvalidValue;
+  const size_t smem_up = 1024 + kStages * (kTM * 128 + BP * 128);
+  const size_t smem_dn = 1024 + kStages * (kKB * 256 + 2 * BP * 128);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(mlp_tc_up_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_up);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mlp_tc_down_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_dn);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int maxU = L.N < L.B * L.cap ? L.N : L.B * L.cap;
+  UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr};
+  mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, 128, smem_up, stream>>>(mW1, mY, ua);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr};
+  dim3 g(L.d / kTM, (maxU + kKChunk - 1) / kKChunk);
+  mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW2, mHi, mLo, da);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_mlp_supported(int B, int d, dv_dtype dt) {
+  return dt != DV_F32 && B >= kTcMinBatch && B <= 32 && d % kTM == 0;
+}
+
+int tc_act_cols(int N) { return (N + kTM - 1) / kTM * kTM; }
+
+cudaError_t launch_sparse_mlp_tc(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
+  if (dt == DV_F16) return L.B <= 16 ? run_tc<__half, 16>(L, hdr, stream) : run_tc<__half, 32>(L, hdr, stream);
+  if (dt == DV_BF16)
+    return L.B <= 16 ? run_tc<__nv_bfloat16, 16>(L, hdr, stream) : run_tc<__nv_bfloat16, 32>(L, hdr, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dv

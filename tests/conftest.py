@@ -11,6 +11,8 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a CUDA device and the built CUDA library")
+    config.addinivalue_line(
+        "markers", "tc: exercises the tcgen05 tensor-core path (also marked gpu)")
 
 
 def pytest_collection_modifyitems(config, items):

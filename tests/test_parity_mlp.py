@@ -29,6 +29,10 @@ CASES = [
     ("batch3_f16",                3, 1024,  4096,  "f16",  205),
     ("batch8_f16",                8, 2048,  8192,  "f16",  410),
     ("batch13_bf16",              13, 1024, 4096,  "bf16", 205),
+    ("batch16_f16_tc",            16, 2048, 8192,  "f16",  410),
+    ("batch32_bf16_opt30b_tc",    32, 7168, 28672, "bf16", 1434),
+    ("batch32_f16_ragged_tc",     32, 768,  3000,  "f16",  77),
+    ("batch8_f32_cuda_cores",     8, 512,   2048,  "f32",  103),
     ("all_neurons_f16",           1, 256,   1024,  "f16",  1024),
     ("one_neuron_f16",            1, 256,   1024,  "f16",  1),
 ]
@@ -59,7 +63,12 @@ def _run(y, W1n, W2n, sets, cap, accumulate=False, base=None):
     return out.cpu().double().numpy(), st, info
 
 
-@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def _marks(case):
+    # batches of 8+ rows in a 16-bit type run on the tcgen05 path
+    return [pytest.mark.tc] if case[1] >= 8 and case[4] != "f32" else []
+
+
+@pytest.mark.parametrize("case", [pytest.param(c, id=c[0], marks=_marks(c)) for c in CASES])
 def test_sparse_mlp_parity(case):
     name, B, d, N, dtype, k = case
     W1n, W2n = _weights(name, d, N, dtype)
