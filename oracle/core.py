@@ -184,15 +184,16 @@ def kv_append(cache: KVCache, y: np.ndarray, Wqkv: np.ndarray, n: int,
         cache.valid[i, n] = True
 
 
-def kv_prefill(cache: KVCache, Wqkv: np.ndarray, n: int) -> None:
-    """A dense prompt of n positions: K/V of every head at positions < n from
-    the stored X (all rows of a head in one product), valid = 1.  Equal to
-    kv_append at every prompt position up to float64 summation order; used
-    to set up timing samples, not by the pins."""
-    for i in range(Wqkv.shape[0]):
+def kv_prefill(cache: KVCache, Wqkv: np.ndarray, n: int,
+               heads: Optional[Sequence[int]] = None) -> None:
+    """A dense prompt of n positions: K/V of the given heads (default: all)
+    at positions < n from the stored X (all rows of a head in one product),
+    valid = 1.  Equal to kv_append at every prompt position up to float64
+    summation order; used to set up large cases, not by the pins."""
+    for i in (range(Wqkv.shape[0]) if heads is None else heads):
         cache.K[i, :n] = round_to(cache.X[:n] @ Wqkv[i, 1].T, cache.dtype)
         cache.V[i, :n] = round_to(cache.X[:n] @ Wqkv[i, 2].T, cache.dtype)
-    cache.valid[:, :n] = True
+        cache.valid[i, :n] = True
 
 
 def kv_repair(cache: KVCache, Wqkv: np.ndarray, n: int,

@@ -38,11 +38,48 @@ def assert_rel_l2(x, ref, dtype: str, what: str = ""):
     return e
 
 
-def within_ulp(got: np.ndarray, exact: np.ndarray, dtype: str, ulps: float = 1.0) -> bool:
-    """|got - exact| <= ulps * ulp(exact) in the storage type (normal range)."""
+def within_ulp(got: np.ndarray, exact: np.ndarray, dtype: str, ulps: float = 1.0,
+               acc_floor=None) -> bool:
+    """|got - exact| <= ulps * ulp(exact) in the storage type (+ acc_floor).
+
+    acc_floor, when given, is an absolute allowance per element for the fp32
+    accumulation of the kernel's dot product (it matters only for values so
+    small that one storage ulp is below the fp32 summation error)."""
     ax = np.maximum(np.abs(exact), 2.0 ** -14)
     ulp = np.exp2(np.floor(np.log2(ax)) - MANT[dtype])
-    return bool(np.all(np.abs(got - exact) <= ulps * ulp))
+    tol = ulps * ulp + (0.0 if acc_floor is None else acc_floor)
+    return bool(np.all(np.abs(got - exact) <= tol))
+
+
+def within_ulp_product(got: np.ndarray, X: np.ndarray, W: np.ndarray, dtype: str) -> bool:
+    """Stored rows got = RNE(X W^T) computed with fp32 accumulation: within one
+    storage ulp of the exact float64 product, plus an fp32 summation allowance
+    of 4 * d * 2^-24 * rms_i(x_i w_i) per element."""
+    exact = X @ W.T
+    d = X.shape[1]
+    rms = np.sqrt(((X * X) @ (W * W).T) / d)
+    return within_ulp(got, exact, dtype, acc_floor=4.0 * d * 2.0 ** -24 * rms)
+
+
+def topk_list_is_valid(lst: np.ndarray, s: np.ndarray, k: int) -> bool:
+    """The kernel's own top-k decision on its own fp32 scores: k ascending
+    unique units, every selected score >= every unselected score, and equal
+    scores resolved in favour of the lower index."""
+    if len(lst) != k or not ascending_unique(lst):
+        return False
+    if k == 0 or k == len(s):
+        return k == 0 or lst.tolist() == list(range(len(s)))
+    sel = np.zeros(len(s), dtype=bool)
+    sel[lst] = True
+    lo = s[sel].min()
+    hi = s[~sel].max()
+    if lo < hi:
+        return False
+    if lo == hi:  # a tie at the boundary: no unselected index below a selected one
+        tied_sel = np.flatnonzero(sel & (s == lo))
+        tied_out = np.flatnonzero(~sel & (s == lo))
+        return tied_sel.max() < tied_out.min()
+    return True
 
 
 def check_selection(gpu: np.ndarray, ref: np.ndarray, s_ref: np.ndarray, mode: str,

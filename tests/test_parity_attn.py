@@ -20,7 +20,7 @@ import torch
 
 import oracle
 from contextual_sparsity_decode_gb300 import binding as dv
-from dvtest import TORCH, assert_rel_l2, f64, within_ulp
+from dvtest import TORCH, assert_rel_l2, f64, within_ulp_product
 from synth import draw
 
 pytestmark = pytest.mark.gpu
@@ -64,8 +64,8 @@ def _check_cache(kv, caches, Wqkv64, pos, sets, dtype, y64):
         for i in S:
             assert np.all(valid[b, i, : p + 1] == 1)
             Xe = X[b, : p + 1]
-            assert within_ulp(K[b, i, : p + 1], Xe @ Wqkv64[i, 1].T, dtype), f"K row, head {i}"
-            assert within_ulp(V[b, i, : p + 1], Xe @ Wqkv64[i, 2].T, dtype), f"V row, head {i}"
+            assert within_ulp_product(K[b, i, : p + 1], Xe, Wqkv64[i, 1], dtype), f"K row, head {i}"
+            assert within_ulp_product(V[b, i, : p + 1], Xe, Wqkv64[i, 2], dtype), f"V row, head {i}"
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
@@ -94,7 +94,7 @@ def test_sparse_attn_parity(case):
         Xe = f64(Xp[b, : prompt[b]])
         for i in range(h):
             assert np.all(valid0[b, i, : prompt[b]] == 1) and np.all(valid0[b, i, prompt[b]:] == 0)
-            assert within_ulp(K0[b, i, : prompt[b]], Xe @ Wqkv64[i, 1].T, dtype)
+            assert within_ulp_product(K0[b, i, : prompt[b]], Xe, Wqkv64[i, 1], dtype)
 
     g = torch.Generator().manual_seed(zlib.crc32(name.encode()))
     cap = h if k == "rnd" else max(1, k)
@@ -162,3 +162,50 @@ def test_position_outside_cache_is_reported():
     st, info = dv.dv_check(ws)
     assert st == 9 and info == n_max      # DV_ERR_POSITION; nothing written
     assert torch.count_nonzero(kv.K) == 0 and torch.count_nonzero(out) == 0
+
+
+#        name                   B  d      h   d_h  dtype   prompt n_max  k
+WIDE = [
+    ("opt30b_b4_bf16",          4, 7168,  56, 128, "bf16", 2047, 2048, 3),
+    ("opt30b_b1_half_bf16",     1, 7168,  56, 128, "bf16", 2047, 2048, 28),
+    ("opt175b_b1_f16",          1, 12288, 96, 128, "f16",  2047, 2048, 20),
+    ("opt175b_b8_f16",          8, 12288, 96, 128, "f16",  2047, 2048, 20),
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=[c[0] for c in WIDE])
+def test_sparse_attn_wide(case):
+    """OPT-30B / OPT-175B widths with a 2047-position dense prompt and one
+    decode step at position 2047 (KV length 2048), several rows per batch
+    with their own head sets.  The oracle's prompt cache is built only for
+    the heads each row selects."""
+    name, B, d, h, d_h, dtype, n_prompt, n_max, k = case
+    dev = "cuda"
+    scale = 1.0 / math.sqrt(d_h)
+    Wqkv, Wo = _layer(name, d, h, d_h, dtype, 0.02)
+    Wqkv64, Wo64 = f64(Wqkv), f64(Wo)
+    kv = dv.KV.empty(B, h, n_max, d_h, d, TORCH[dtype], dev)
+    Xp = draw((B, n_prompt, d), 1.0, 304, name + "/X", dtype)
+    kv.X[:, :n_prompt].copy_(Xp.to(dev))
+    pos = torch.full((B,), n_prompt, dtype=torch.int32, device=dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, h, n_max))
+    all_heads = torch.arange(h, dtype=torch.int32, device=dev).repeat(B, 1)
+    dv.dv_kv_repair(kv, Wqkv.to(dev), pos, all_heads, torch.full((B,), h, dtype=torch.int32, device=dev), ws)
+    assert dv.dv_check(ws)[0] == 0
+    g = torch.Generator().manual_seed(zlib.crc32(name.encode()))
+    sets = [_subset(g, h, k) for _ in range(B)]
+    idx = torch.stack(sets).to(dev)
+    cnt = torch.full((B,), k, dtype=torch.int32, device=dev)
+    y = draw((B, d), 1.0, 304, name + "/y", dtype)
+    out = torch.zeros(B, d, device=dev)
+    ws2 = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, k, n_max))
+    dv.dv_sparse_attn(y.to(dev), Wqkv.to(dev), Wo.to(dev), kv, pos, idx, cnt, scale, out, ws2)
+    st, info = dv.dv_check(ws2)
+    assert st == 0, (st, info)
+    got, y64 = f64(out), f64(y)
+    for b in range(B):
+        c = oracle.KVCache.empty(h, n_max, d_h, d, dtype)
+        c.X[:n_prompt] = f64(Xp[b])
+        oracle.kv_prefill(c, Wqkv64, n_prompt, heads=sets[b].tolist())
+        ref = oracle.sparse_attn(y64[b], Wqkv64, Wo64, c, n_prompt, sets[b].tolist(), scale)
+        assert_rel_l2(got[b], ref, dtype, f"{name} row {b}")

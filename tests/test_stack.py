@@ -2,10 +2,14 @@
 CUDA-graph replay) with the oracle's free-running decode_stack.
 
 Both sides start from the same residual input and prompt embeddings and run
-their own predictors, so index lists are compared with the 1e-5 window rule;
-a list that differs inside the window (a legitimate near-tie flip) makes the
-two trajectories diverge, after which the comparison stops.  Outputs are
-compared by relative L2 (1e-3 for fp16 storage)."""
+their own predictors on their own layer inputs.  Those inputs agree only to
+the storage type's rounding (an element of LN(r) can land one fp16 ulp apart
+when r differs in its last fp32 bits), which moves scores by up to ~1e-4, so
+index lists are compared with a 2e-4 window around the boundary here (the
+1e-5 rule of the predictor tests assumes identical inputs).  A list that
+differs inside the window (a near-tie flip) makes the trajectories diverge,
+after which the comparison stops.  Outputs are compared by relative L2
+(1e-3 for 16-bit storage)."""
 
 import math
 
@@ -20,6 +24,8 @@ from dvtest import assert_rel_l2, check_selection, f64
 from synth import Workload, embeddings, layer_weights, residual_input
 
 pytestmark = pytest.mark.gpu
+
+STACK_WINDOW = 2e-4
 
 
 def _run_stack(w: Workload, steps: int, graph_from: int = 1):
@@ -60,8 +66,8 @@ def _run_stack(w: Workload, steps: int, graph_from: int = 1):
             gM = dec.neur_idx[l][0, : int(dec.neur_cnt[l][0])].cpu().numpy()
             _, sA, _ = oracle.predict(trace[l], layers64[l]["PA1t"], layers64[l]["PA2t"], "topk", w.k_heads)
             _, sM, _ = oracle.predict(trace[l], layers64[l]["PM1t"], layers64[l]["PM2t"], "topk", w.k_neurons)
-            flips = check_selection(gA, sets[l][0], sA[0], "topk", w.k_heads)
-            flips += check_selection(gM, sets[l][1], sM[0], "topk", w.k_neurons)
+            flips = check_selection(gA, sets[l][0], sA[0], "topk", w.k_heads, window=STACK_WINDOW)
+            flips += check_selection(gM, sets[l][1], sM[0], "topk", w.k_neurons, window=STACK_WINDOW)
             if flips:
                 diverged = True
                 break
