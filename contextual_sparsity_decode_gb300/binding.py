@@ -33,7 +33,7 @@ _DT = {torch.float32: DV_F32, torch.float16: DV_F16, torch.bfloat16: DV_BF16}
 # every entry point declared in include/dv.h
 EXPORTS = (
     "dv_status_str", "dv_last_cuda_error", "dv_version", "dv_workspace_init", "dv_check",
-    "dv_predict_workspace_size", "dv_predict", "dv_lookahead",
+    "dv_predict_workspace_size", "dv_predict", "dv_lookahead", "dv_predict_static",
     "dv_sparse_mlp_workspace_size", "dv_sparse_mlp",
     "dv_sparse_attn_workspace_size", "dv_sparse_attn", "dv_kv_repair",
     "dv_layernorm", "dv_positions_advance",
@@ -73,6 +73,8 @@ _SIGS = {
                    _c_int),
     "dv_lookahead": ([_vp, _c_int, _c_int, _c_int, ctypes.POINTER(dv_predictor), _c_int, _vp, _sz,
                       _vp, _vp, _vp], _c_int),
+    "dv_predict_static": ([_vp, _c_int, _c_int, _c_int, ctypes.POINTER(dv_predictor), _c_int, _vp],
+                          _c_int),
     "dv_sparse_mlp_workspace_size": ([_c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_sz)], _c_int),
     "dv_sparse_mlp": ([_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp, _c_int, _vp, _c_int,
                        _vp, _sz, _vp], _c_int),
@@ -211,6 +213,15 @@ def dv_predict(y: torch.Tensor, preds: Sequence[Predictor], ws: torch.Tensor, st
     B, d = y.shape
     _ok(lib().dv_predict(_ptr(y), B, d, _dt(y), arr, n, _ptr(ws), ws.numel(), _stream(stream)),
         "dv_predict")
+
+
+def dv_predict_static(y: torch.Tensor, preds: Sequence[Predictor], stream=None):
+    """dv_predict without a workspace: the library's fixed scratch array is
+    used instead (for callers that cannot allocate; see dv.h for limits)."""
+    arr, n = _preds(preds)
+    B, d = y.shape
+    _ok(lib().dv_predict_static(_ptr(y), B, d, _dt(y), arr, n, _stream(stream)),
+        "dv_predict_static")
 
 
 def dv_lookahead(y: torch.Tensor, preds: Sequence[Predictor], ws: torch.Tensor,

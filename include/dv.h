@@ -158,6 +158,30 @@ dv_status dv_lookahead(const void* y, int B, int d, dv_dtype dt,
                        cudaEvent_t input_ready, cudaStream_t side,
                        cudaEvent_t done);
 
+/* Sparsity prediction without a caller workspace.  The pages have no
+ * counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory -- for example a plugin inside a serving engine
+ * that owns every device allocation, or a latency-critical loop where a
+ * cudaMalloc (which can synchronise the device) is not allowed.
+ *
+ * Computes exactly what dv_predict computes, with the same arguments minus
+ * the workspace.  Its scratch lives in a fixed array inside the library
+ * (about 1.1 MB; every GPU that loads the library holds one until the
+ * process exits).  Limits: B <= 4, r <= 1024 and N <= 32768 per predictor;
+ * larger shapes are rejected with DV_ERR_WORKSPACE before anything runs.
+ * Nothing is allocated or freed: no cudaMalloc, no cudaFree.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call, on any stream, shares the one array and overwrites what the
+ *    previous call left there: calls whose work overlaps on the GPU race and
+ *    give wrong results.  Serialise them (one stream, or events).
+ *  - Device-side conditions are not reported: a threshold list longer than
+ *    cap is truncated to cap entries as in dv_predict, with no error word to
+ *    read back. */
+dv_status dv_predict_static(const void* y, int B, int d, dv_dtype dt,
+                            const dv_predictor* preds, int n_preds,
+                            cudaStream_t stream);
+
 /* ------------------------------------------------------------ sparse MLP */
 
 dv_status dv_sparse_mlp_workspace_size(int B, int d, int N, int cap,
