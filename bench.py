@@ -44,6 +44,8 @@ def _args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="opt13b_stack_fp16")
+    p.add_argument("--layers", type=int, default=None,
+                   help="run only the first L layers of the workload (small profiling cases)")
     p.add_argument("--cpu-layers", type=int, default=2,
                    help="layers of the workload in the oracle's timed sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -149,9 +151,11 @@ def _peaks():
 
 # ----------------------------------------------------------------- workload
 
-def _workload(name):
+def _workload(name, layers=None):
     from synth import WORKLOADS
     w = WORKLOADS[name]
+    if layers is not None:
+        w = w.with_(layers=max(1, min(layers, w.layers)))
     return w
 
 
@@ -189,7 +193,7 @@ def run_ours(args, rank, world, local):
     from contextual_sparsity_decode_gb300.stack import SparseDecoder
     from synth import embeddings, layer_weights, residual_input
 
-    w = _workload(args.workload)
+    w = _workload(args.workload, args.layers)
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     dv.lib()
@@ -343,7 +347,7 @@ def cpu_sample(args, w, layers=None):
 
 def run_reference(args, rank, world):
     import oracle
-    w = _workload(args.workload)
+    w = _workload(args.workload, args.layers)
     nl = max(1, min(args.cpu_layers, w.layers))
     layers64, caches, r = _oracle_setup(w, None, nl)
     scale = 1.0 / math.sqrt(w.d_h)
