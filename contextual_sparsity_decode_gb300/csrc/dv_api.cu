@@ -371,7 +371,8 @@ dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h, const void
 dv_status dv_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtype dt,
                        cudaStream_t stream) {
   if (!dtype_ok(dt)) return DV_ERR_DTYPE;
-  if (!x || !y || B < 1 || d < 1 || !(eps >= 0.f)) return DV_ERR_INVALID_ARG;
+  if (!x || !y || B < 1 || d < 4 || d > 16384 || d % 4 || !(eps >= 0.f)) return DV_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 7u)) return DV_ERR_INVALID_ARG;
   cudaError_t e = launch_layernorm(x, B, d, eps, y, dt, stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);
 }

@@ -155,6 +155,15 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   return v;
 }
 
+// Store a float into CTA `rank`'s shared memory at the address of `local`
+// (made visible to that CTA by the next cluster barrier's release/acquire).
+__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
+  uint32_t saddr = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(saddr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void atomic_add_f32x4(float* dst, float a, float b, float c, float d) {
   atomicAdd(reinterpret_cast<float4*>(dst), make_float4(a, b, c, d));
 }

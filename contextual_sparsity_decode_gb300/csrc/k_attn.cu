@@ -5,16 +5,16 @@
 // recomputed when selected later).
 //
 // One decode step is three kernels:
-//   attn_qkv     one warp per row of W_i^{Q,K,V} of each selected head (head
-//                rows are contiguous: Wqkv[i][m][t][:]).  The warp streams its
-//                row once and dots it with every vector that needs it: the
-//                current token(s) and, for K/V rows, the stored embeddings
-//                X[j] of positions whose K/V were skipped (fused repair, so a
-//                repair costs no extra weight traffic).
+//   attn_qkv     a CTA holds a few rows of W_i^{Q,K,V} of one selected head
+//                in registers (head rows are contiguous: Wqkv[i][m][t][:]) and
+//                dots them with every vector that needs them: the current
+//                token(s) and, for K/V rows, the stored embeddings X[j] of
+//                positions whose K/V were skipped (fused repair, so a repair
+//                costs no extra weight traffic).
 //   attn_decode  split-KV softmax: one CTA per (row, head, 64-position chunk),
-//                online max/sum per warp, partials combined by the last CTA of
-//                each head (ticket counter, no spin wait).  Also appends X[pos]
-//                and updates the valid flags.
+//                every K/V load of a warp issued before the first use, partials
+//                combined by the last CTA of each head (ticket counter, no spin
+//                wait).  Also appends X[pos] and updates the valid flags.
 //   attn_out     out += sum_i H_i W_i^O as a weighted sum of the selected
 //                heads' W^O rows, column-sliced across CTAs, fp32 atomics.
 // The standalone repair (dv_kv_repair, e.g. a dense prefill) uses a tiled
@@ -25,10 +25,9 @@
 namespace dv {
 namespace {
 
-constexpr int kEntCap = 8192;      // vector entries per flush in attn_qkv
-constexpr int kVG = 16;            // vectors dotted per pass over a weight row
 constexpr int kCur = 1 << 30;      // entry flag: the current token (vector = y_b)
 constexpr int kCH = kAttnChunk;
+constexpr int kMaxChunks = 65536 / kAttnChunk;  // n_max <= 65536
 
 struct AttnArgs {
   const void* y;
@@ -71,82 +70,135 @@ __device__ __forceinline__ int row_pos(const AttnArgs& a, int b) {
 
 // ---------------------------------------------------------------------------
 // attn_qkv
+//
+// A CTA owns rpc = (256 / TPR) * kQR consecutive rows of one selected head's
+// W^{Q,K,V} block (rpc divides d_h, so a CTA never straddles Q/K/V); a group
+// of TPR threads shares kQR rows, each thread holding kQC 16-byte chunks of
+// each.  All weight loads are issued before any entry is processed, and the
+// registers are reused for every vector the rows are dotted with: the
+// current token of every batch row that selected the head, and (K/V rows)
+// the stored embedding X[j] of every position j < pos whose K/V were skipped.
+
+constexpr int kQC = 4;      // chunks per thread per pass over a row
+constexpr int kQR = 4;      // rows per thread group (divides d_h)
+constexpr int kNE = 4;      // vectors per group of entries
+constexpr int kWin = 4096;  // positions scanned per repair window (256 x 16)
+
+int qkv_tpr_log2(int chunks) {
+  int l = 5;
+  while (l < 8 && (1 << l) * kQC < chunks) ++l;
+  return l;
+}
 
 template <typename T>
-__device__ void qkv_dots(const AttnArgs& a, const T* wrow, int m, int t, int i, int u,
-                         const int* ent, int n_ent) {
+__device__ __forceinline__ void qkv_load_w(const T* wbase, int d, int C, int cb, int tt, int tpr,
+                                           uint4 (&w)[kQR][kQC]) {
   constexpr int V = Elem<T>::kVec;
-  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < kQR; ++k)
+#pragma unroll
+    for (int j = 0; j < kQC; ++j) {
+      const int c = cb + tt + j * tpr;
+      if (c < C) w[k][j] = ld_stream(wbase + (size_t)k * d + (size_t)c * V);
+    }
+}
+
+// Dots the CTA's rows with entries ent[0..n) and stores the results (q in
+// fp32, K/V rounded to the storage type).  Called by all threads.
+template <typename T>
+__device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)[kQR][kQC],
+                            bool one_pass, const T* wbase, int tl, int m, int tbase, int i, int u,
+                            float (&red)[8][kQR][kNE]) {
+  constexpr int V = Elem<T>::kVec;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tpr = 1 << tl, RS = 256 >> tl, tt = tid & (tpr - 1);
   const int C = a.d / V;
   const T* y = static_cast<const T*>(a.y);
   const T* X = static_cast<const T*>(a.X);
-  for (int g0 = 0; g0 < n_ent; g0 += kVG) {
-    const int ng = min(kVG, n_ent - g0);
-    float acc[kVG];
+  for (int g0 = 0; g0 < n; g0 += kNE) {
+    const int ne = min(kNE, n - g0);
+    float acc[kQR][kNE];
 #pragma unroll
-    for (int e = 0; e < kVG; ++e) acc[e] = 0.f;
-    for (int s0 = 0; s0 < C; s0 += 256) {
-      uint4 wv[8];
+    for (int k = 0; k < kQR; ++k)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = s0 + lane + 32 * k;
-        if (c < C) wv[k] = ld_stream(wrow + (size_t)c * V);
-      }
+      for (int e = 0; e < kNE; ++e) acc[k][e] = 0.f;
+    for (int cb = 0; cb < C; cb += tpr * kQC) {
+      if (!one_pass) qkv_load_w<T>(wbase, a.d, C, cb, tt, tpr, w);
 #pragma unroll
-      for (int e = 0; e < kVG; ++e) {
-        if (e < ng) {
+      for (int j = 0; j < kQC; ++j) {
+        const int c = cb + tt + j * tpr;
+        if (c >= C) break;
+#pragma unroll
+        for (int e = 0; e < kNE; ++e) {
+          if (e >= ne) break;
           const int en = ent[g0 + e];
-          const int b = (en >> 20) & 1023, j = en & 0xfffff;
-          const T* vec = (en & kCur) ? y + (size_t)b * a.d
-                                     : X + ((size_t)b * a.n_max + j) * a.d;
+          const int b = (en >> 20) & 1023, jp = en & 0xfffff;
+          const T* vec = (en & kCur) ? y + (size_t)b * a.d : X + ((size_t)b * a.n_max + jp) * a.d;
+          float xf[V];
+          unpack<T>(ld_cached(vec + (size_t)c * V), xf);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int c = s0 + lane + 32 * k;
-            if (c < C) {
-              float wf[V], xf[V];
-              unpack<T>(wv[k], wf);
-              unpack<T>(ld_cached(vec + (size_t)c * V), xf);
+          for (int k = 0; k < kQR; ++k) {
+            float wf[V];
+            unpack<T>(w[k][j], wf);
 #pragma unroll
-              for (int v = 0; v < V; ++v) acc[e] = fmaf(wf[v], xf[v], acc[e]);
-            }
+            for (int v = 0; v < V; ++v) acc[k][e] = fmaf(wf[v], xf[v], acc[k][e]);
           }
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < kVG; ++e) {
-      if (e < ng) {
-        const float s = warp_sum(acc[e]);
-        if (lane == 0) {
-          const int en = ent[g0 + e];
-          const int b = (en >> 20) & 1023, j = en & 0xfffff;
-          if (m == 0) {
-            a.q[((size_t)b * a.capU + u) * a.d_h + t] = s;
-          } else {
-            T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
-            dst[(((size_t)b * a.h + i) * a.n_max + j) * a.d_h + t] = Elem<T>::from_f(s);
-          }
-        }
+    for (int k = 0; k < kQR; ++k)
+#pragma unroll
+      for (int e = 0; e < kNE; ++e) {
+        if (e >= ne) break;
+        const float z = warp_sum(acc[k][e]);
+        if (lane == 0) red[wid][k][e] = z;
+      }
+    __syncthreads();
+    const int nw = tpr >> 5;
+    for (int q = tid; q < RS * kQR * ne; q += 256) {
+      const int sl = q / (kQR * ne), k = (q / ne) % kQR, e = q % ne;
+      float z = 0.f;
+      for (int x = 0; x < nw; ++x) z += red[sl * nw + x][k][e];
+      const int en = ent[g0 + e];
+      const int b = (en >> 20) & 1023, jp = en & 0xfffff;
+      const int t = tbase + sl * kQR + k;
+      if (m == 0) {
+        a.q[((size_t)b * a.capU + u) * a.d_h + t] = z;
+      } else {
+        T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
+        dst[(((size_t)b * a.h + i) * a.n_max + jp) * a.d_h + t] = Elem<T>::from_f(z);
       }
     }
+    __syncthreads();  // red is rewritten by the next group
   }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) attn_qkv_kernel(AttnArgs a, int RG) {
-  __shared__ int ent[kEntCap];
+__global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, int tl) {
+  constexpr int V = Elem<T>::kVec;
+  __shared__ int ent[kWin];
   __shared__ int n_ent;
-  const int tid = threadIdx.x, wid = tid >> 5;
+  __shared__ float red[8][kQR][kNE];
+  const int tid = threadIdx.x;
+  const int tpr = 1 << tl, RS = 256 >> tl, slot = tid >> tl, tt = tid & (tpr - 1);
+  const int rpc = RS * kQR;
   const int u = blockIdx.x / RG, rg = blockIdx.x % RG;
+  const int i = a.U[u];  // u < capU: in bounds; loaded together with the count
   if (u >= union_count(a)) return;
-  const int i = a.U[u];
   if (i < 0 || i >= a.h) {
     if (tid == 0 && rg == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
     return;
   }
-  const int m = (rg * 8) / a.d_h;  // uniform over the CTA: 8 rows never straddle Q/K/V
-  const int t = rg * 8 + wid - m * a.d_h;
-  const T* wrow = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + t) * a.d;
+  const int r0 = rg * rpc;        // first row of the CTA within the head's 3 d_h rows
+  const int m = r0 / a.d_h;       // 0 = Q, 1 = K, 2 = V
+  const int tbase = r0 - m * a.d_h;
+  const T* wbase = static_cast<const T*>(a.Wqkv) +
+                   ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
+  const int C = a.d / V;
+  const bool one_pass = C <= tpr * kQC;
+  uint4 w[kQR][kQC];
+  if (one_pass) qkv_load_w<T>(wbase, a.d, C, 0, tt, tpr, w);
 
   if (tid == 0) n_ent = 0;
   __syncthreads();
@@ -155,23 +207,16 @@ __global__ void __launch_bounds__(256) attn_qkv_kernel(AttnArgs a, int RG) {
     if (p >= 0 && member_of(a, b, i)) ent[atomicAdd(&n_ent, 1)] = kCur | (b << 20) | p;
   }
   __syncthreads();
-  if (m == 0) {
-    qkv_dots<T>(a, wrow, m, t, i, u, ent, n_ent);
-    return;
-  }
-  // K/V rows: append the positions whose K/V were skipped, flushing when full
+  qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red);
+  if (m == 0) return;
+  // K/V rows: positions whose K/V were skipped, one window of 4096 at a time
   for (int b = 0; b < a.B; ++b) {
     const int p = row_pos(a, b);
     if (p < 0 || !member_of(a, b, i)) continue;
     const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
-    for (int base = 0; base < p; base += 4096) {
+    for (int base = 0; base < p; base += kWin) {
+      if (tid == 0) n_ent = 0;
       __syncthreads();
-      if (n_ent + 4096 > kEntCap) {
-        qkv_dots<T>(a, wrow, m, t, i, u, ent, n_ent);
-        __syncthreads();
-        if (tid == 0) n_ent = 0;
-        __syncthreads();
-      }
       const int j0 = base + tid * 16;
       if (j0 < p) {
         const uint4 v4 = *reinterpret_cast<const uint4*>(vr + j0);
@@ -183,47 +228,50 @@ __global__ void __launch_bounds__(256) attn_qkv_kernel(AttnArgs a, int RG) {
             ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
         }
       }
+      __syncthreads();
+      qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red);
     }
   }
-  __syncthreads();
-  qkv_dots<T>(a, wrow, m, t, i, u, ent, n_ent);
 }
 
 // ---------------------------------------------------------------------------
 // attn_decode
 
-template <typename T> struct KvLoad;
-// E consecutive elements of a K or V row for one lane, as floats.
-template <> struct KvLoad<float> {
-  template <int E> static __device__ __forceinline__ void get(const float* p, float* f) {
-    if constexpr (E == 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-      f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-    } else {
-      const float2 v = __ldg(reinterpret_cast<const float2*>(p));
-      f[0] = v.x; f[1] = v.y;
-    }
+// E consecutive elements of a K or V row for one lane, loaded raw (one
+// 4..16-byte load) and converted to floats at use.
+template <typename T, int E> struct KvRaw;
+template <> struct KvRaw<float, 4> {
+  using type = float4;
+  static __device__ __forceinline__ type load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+  static __device__ __forceinline__ void to_f(const type& v, float* f) { f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w; }
+};
+template <> struct KvRaw<float, 2> {
+  using type = float2;
+  static __device__ __forceinline__ type load(const float* p) { return __ldg(reinterpret_cast<const float2*>(p)); }
+  static __device__ __forceinline__ void to_f(const type& v, float* f) { f[0] = v.x; f[1] = v.y; }
+};
+template <typename H16> struct KvRaw16x4 {
+  using type = uint2;
+  static __device__ __forceinline__ type load(const H16* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+  static __device__ __forceinline__ void to_f(const type& v, float* f) {
+    float t[8];
+    unpack<H16>(make_uint4(v.x, v.y, 0u, 0u), t);
+    f[0] = t[0]; f[1] = t[1]; f[2] = t[2]; f[3] = t[3];
   }
 };
-template <typename H16> struct KvLoad16 {
-  template <int E> static __device__ __forceinline__ void get(const H16* p, float* f) {
-    if constexpr (E == 4) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-      uint4 q = make_uint4(v.x, v.y, 0u, 0u);
-      float t[8];
-      unpack<H16>(q, t);
-      f[0] = t[0]; f[1] = t[1]; f[2] = t[2]; f[3] = t[3];
-    } else {
-      const uint32_t v = __ldg(reinterpret_cast<const unsigned int*>(p));
-      uint4 q = make_uint4(v, 0u, 0u, 0u);
-      float t[8];
-      unpack<H16>(q, t);
-      f[0] = t[0]; f[1] = t[1];
-    }
+template <typename H16> struct KvRaw16x2 {
+  using type = uint32_t;
+  static __device__ __forceinline__ type load(const H16* p) { return __ldg(reinterpret_cast<const unsigned int*>(p)); }
+  static __device__ __forceinline__ void to_f(const type& v, float* f) {
+    float t[8];
+    unpack<H16>(make_uint4(v, 0u, 0u, 0u), t);
+    f[0] = t[0]; f[1] = t[1];
   }
 };
-template <> struct KvLoad<__half> : KvLoad16<__half> {};
-template <> struct KvLoad<__nv_bfloat16> : KvLoad16<__nv_bfloat16> {};
+template <> struct KvRaw<__half, 4> : KvRaw16x4<__half> {};
+template <> struct KvRaw<__half, 2> : KvRaw16x2<__half> {};
+template <> struct KvRaw<__nv_bfloat16, 4> : KvRaw16x4<__nv_bfloat16> {};
+template <> struct KvRaw<__nv_bfloat16, 2> : KvRaw16x2<__nv_bfloat16> {};
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
@@ -240,7 +288,19 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     constexpr int V = Elem<T>::kVec;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.y) + (size_t)b * a.d);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + ((size_t)b * a.n_max + p) * a.d);
-    for (int k = tid; k < a.d / V; k += blockDim.x) dst[k] = src[k];
+    for (int k0 = tid; k0 < a.d / V; k0 += 8 * blockDim.x) {  // 8 loads in flight, then 8 stores
+      uint4 t8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int k = k0 + q * blockDim.x;
+        if (k < a.d / V) t8[q] = __ldg(src + k);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int k = k0 + q * blockDim.x;
+        if (k < a.d / V) dst[k] = t8[q];
+      }
+    }
     for (int i = tid; i < a.h; i += blockDim.x) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
     __syncthreads();
     const int cnt = max(0, min(a.head_count[b], a.cap));
@@ -250,9 +310,11 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     }
     return;
   }
-  const int cnt = max(0, min(a.head_count[b], a.cap));
-  if (s >= cnt || p < 0) return;
+  // count and head index are independent loads (s < cap keeps the index in bounds)
+  const int cnt_raw = a.head_count[b];
   const int i = a.head_idx[(size_t)b * a.cap + s];
+  const int cnt = max(0, min(cnt_raw, a.cap));
+  if (s >= cnt || p < 0) return;
   if (i < 0 || i >= a.h) {
     if (tid == 0 && c == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
     return;
@@ -265,6 +327,7 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 
   __shared__ float sm[4], sl[4];
   __shared__ float sacc[4][DH];
+  __shared__ float wts[kMaxChunks];
   __shared__ int is_last;
 
   float qr[E];
@@ -274,23 +337,57 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
 
   const T* Kr = static_cast<const T*>(a.K) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
   const T* Vr = static_cast<const T*>(a.V) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
+  // each warp owns kCH/4 consecutive positions, loaded kPB at a time with
+  // every K and V load of the batch issued before the first use
+  constexpr int kPW = kCH / 4;
+  constexpr int kPB = sizeof(T) == 2 ? kPW : kPW / 2;
+  using Raw = typename KvRaw<T, E>::type;
   float mw = -INFINITY, lw = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int j = j0 + wid; j < j1; j += 4) {
-    float kf[E], vf[E];
-    KvLoad<T>::template get<E>(Kr + (size_t)j * DH, kf);
-    KvLoad<T>::template get<E>(Vr + (size_t)j * DH, vf);
-    float dot = 0.f;
+  const int jw = j0 + wid * kPW;
+#pragma unroll 1
+  for (int jb = jw; jb < min(j1, jw + kPW); jb += kPB) {
+    Raw kraw[kPB], vraw[kPB];
 #pragma unroll
-    for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
-    const float logit = warp_sum(dot);
-    const float mn = fmaxf(mw, logit);
-    const float corr = expf(mw - mn);
-    const float pj = expf(logit - mn);
-    lw = lw * corr + pj;
+    for (int s2 = 0; s2 < kPB; ++s2) {
+      const int j = jb + s2;
+      if (j < j1) {
+        kraw[s2] = KvRaw<T, E>::load(Kr + (size_t)j * DH);
+        vraw[s2] = KvRaw<T, E>::load(Vr + (size_t)j * DH);
+      }
+    }
+    float lg[kPB];
+    float mb = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, vf[e], acc[e] * corr);
+    for (int s2 = 0; s2 < kPB; ++s2) {
+      lg[s2] = -INFINITY;
+      if (jb + s2 < j1) {
+        float kf[E];
+        KvRaw<T, E>::to_f(kraw[s2], kf);
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
+        lg[s2] = warp_sum(dot);
+        mb = fmaxf(mb, lg[s2]);
+      }
+    }
+    const float mn = fmaxf(mw, mb);
+    const float corr = expf(mw - mn);  // 0 on the first batch (mw = -inf)
+    lw *= corr;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= corr;
+#pragma unroll
+    for (int s2 = 0; s2 < kPB; ++s2) {
+      if (jb + s2 < j1) {
+        const float pj = expf(lg[s2] - mn);
+        float vf[E];
+        KvRaw<T, E>::to_f(vraw[s2], vf);
+        lw += pj;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
+      }
+    }
     mw = mn;
   }
   if (lane == 0) { sm[wid] = mw; sl[wid] = lw; }
@@ -328,20 +425,30 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
+  // combine the chunks: per-chunk weights w_k = exp(M_k - M) in shared memory,
+  // then one pass over the partial numerators with 16 loads in flight
   const float* pb = a.part + ((size_t)b * a.cap + s) * a.n_chunks * (DH + 2);
-  float Mg = -INFINITY;
-  for (int k = 0; k < nch; ++k) Mg = fmaxf(Mg, __ldcg(pb + (size_t)k * (DH + 2)));
-  float den = 0.f;
-  for (int k = 0; k < nch; ++k) {
+  float mloc = -INFINITY;
+  for (int k = tid; k < nch; k += blockDim.x) mloc = fmaxf(mloc, __ldcg(pb + (size_t)k * (DH + 2)));
+  mloc = warp_max(mloc);
+  if (lane == 0) sm[wid] = mloc;
+  __syncthreads();
+  const float Mg = fmaxf(fmaxf(sm[0], sm[1]), fmaxf(sm[2], sm[3]));
+  float lloc = 0.f;
+  for (int k = tid; k < nch; k += blockDim.x) {
     const float* pk = pb + (size_t)k * (DH + 2);
-    den += __ldcg(pk + 1) * expf(__ldcg(pk) - Mg);
+    const float wk = expf(__ldcg(pk) - Mg);
+    wts[k] = wk;
+    lloc += __ldcg(pk + 1) * wk;
   }
+  lloc = warp_sum(lloc);
+  if (lane == 0) sl[wid] = lloc;
+  __syncthreads();
+  const float den = (sl[0] + sl[1]) + (sl[2] + sl[3]);
   for (int t = tid; t < DH; t += blockDim.x) {
     float num = 0.f;
-    for (int k = 0; k < nch; ++k) {
-      const float* pk = pb + (size_t)k * (DH + 2);
-      num += __ldcg(pk + 2 + t) * expf(__ldcg(pk) - Mg);
-    }
+#pragma unroll 16
+    for (int k = 0; k < nch; ++k) num += __ldcg(pb + (size_t)k * (DH + 2) + 2 + t) * wts[k];
     a.H[((size_t)b * a.capU + u) * DH + t] = num / den;
   }
   if (tid == 0) a.ticket[(size_t)b * a.cap + s] = 0;
@@ -368,6 +475,8 @@ SlicePlan plan_slices(int chunks) {
   return best;
 }
 
+constexpr int kOL = 12;  // W^O row loads in flight per thread
+
 template <typename T, int BT>
 __global__ void __launch_bounds__(256) attn_out_kernel(AttnArgs a, int CS, int CPR, int b0) {
   constexpr int V = Elem<T>::kVec;
@@ -386,11 +495,12 @@ __global__ void __launch_bounds__(256) attn_out_kernel(AttnArgs a, int CS, int C
   for (int b = 0; b < BT; ++b)
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[b][v] = 0.f;
-  for (int r = r0 + gi; r < r1; r += 4 * NG) {
-    uint4 wv[4];
-    int ii[4], uu[4], tt[4];
+  // every thread issues up to kOL row loads before using any
+  for (int r = r0 + gi; r < r1; r += kOL * NG) {
+    uint4 wv[kOL];
+    int ii[kOL], uu[kOL], tt[kOL];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kOL; ++k) {
       const int rr = r + k * NG;
       ii[k] = -1;
       if (rr < r1) {
@@ -404,7 +514,7 @@ __global__ void __launch_bounds__(256) attn_out_kernel(AttnArgs a, int CS, int C
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kOL; ++k) {
       if (ii[k] < 0) continue;
       float wf[V];
       unpack<T>(wv[k], wf);
@@ -579,8 +689,9 @@ template <typename T>
 cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t stream) {
   AttnArgs a = make_args(L, hdr);
   // 1. projections + fused repair
-  const int RG = 3 * a.d_h / 8;
-  attn_qkv_kernel<T><<<a.capU * RG, 256, 0, stream>>>(a, RG);
+  const int tl = qkv_tpr_log2(a.d / Elem<T>::kVec);
+  const int RG = 3 * a.d_h / ((256 >> tl) * kQR);
+  attn_qkv_kernel<T><<<a.capU * RG, 256, 0, stream>>>(a, RG, tl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 2. split-KV softmax, last-CTA combine, cache bookkeeping

@@ -7,44 +7,79 @@ namespace dv {
 namespace {
 
 constexpr int kLnThreads = 512;
+constexpr int kLnVec = 8;  // float4 per thread: d <= 512 * 4 * 8 = 16384
 
-// y = (x - mean) / sqrt(var + eps) per row, rounded to the storage type.
+__device__ __forceinline__ float block_sum_ln(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];  // same order in every thread
+  __syncthreads();
+  return t;
+}
+
+template <typename T> struct Store4;
+template <> struct Store4<float> {
+  static __device__ __forceinline__ void put(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+};
+template <> struct Store4<__half> {
+  static __device__ __forceinline__ void put(__half* p, float4 v) {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+template <> struct Store4<__nv_bfloat16> {
+  static __device__ __forceinline__ void put(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+};
+
+// y = (x - mean) / sqrt(var + eps) per row, rounded to the storage type.  The
+// row is read once into registers (one round trip); mean and variance are
+// two block reductions over the registers.
 template <typename T>
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float* x, int d, float eps, T* y) {
   __shared__ float red[kLnThreads / 32];
-  __shared__ float stat;
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const float* xr = x + (size_t)b * d;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)b * d);
+  const int n4 = d / 4;
+  float4 v[kLnVec];
+#pragma unroll
+  for (int k = 0; k < kLnVec; ++k) {
+    const int c = tid + k * kLnThreads;
+    v[k] = c < n4 ? __ldcg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float s = 0.f;
-  for (int c = tid; c < d; c += kLnThreads) s += xr[c];
-  s = warp_sum(s);
-  if (lane == 0) red[wid] = s;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
-    stat = t / (float)d;
-  }
-  __syncthreads();
-  const float mean = stat;
+#pragma unroll
+  for (int k = 0; k < kLnVec; ++k) s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+  const float mean = block_sum_ln(s, red) / (float)d;
   float q = 0.f;
-  for (int c = tid; c < d; c += kLnThreads) {
-    const float v = xr[c] - mean;
-    q = fmaf(v, v, q);
+#pragma unroll
+  for (int k = 0; k < kLnVec; ++k) {
+    if (tid + k * kLnThreads < n4) {
+      const float a0 = v[k].x - mean, a1 = v[k].y - mean, a2 = v[k].z - mean, a3 = v[k].w - mean;
+      q = fmaf(a0, a0, q); q = fmaf(a1, a1, q); q = fmaf(a2, a2, q); q = fmaf(a3, a3, q);
+    }
   }
-  q = warp_sum(q);
-  __syncthreads();
-  if (lane == 0) red[wid] = q;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
-    stat = 1.f / sqrtf(t / (float)d + eps);
-  }
-  __syncthreads();
-  const float inv = stat;
+  const float inv = 1.f / sqrtf(block_sum_ln(q, red) / (float)d + eps);
   T* yr = y + (size_t)b * d;
-  for (int c = tid; c < d; c += kLnThreads) yr[c] = Elem<T>::from_f((xr[c] - mean) * inv);
+#pragma unroll
+  for (int k = 0; k < kLnVec; ++k) {
+    const int c = tid + k * kLnThreads;
+    if (c < n4)
+      Store4<T>::put(yr + 4 * c, make_float4((v[k].x - mean) * inv, (v[k].y - mean) * inv,
+                                             (v[k].z - mean) * inv, (v[k].w - mean) * inv));
+  }
 }
 
 __global__ void positions_kernel(int32_t* pos, int B, int lo, int hi) {

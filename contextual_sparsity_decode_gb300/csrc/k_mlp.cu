@@ -8,18 +8,20 @@
 // weights, 16-byte aligned), so every gathered neuron is two contiguous rows
 // ("Memory coalescing", §3.3).  A thread-block cluster of CS CTAs splits the
 // d columns; cluster g owns a contiguous share of the selected neurons:
-//   phase 1  each CTA dots its column slice of W^1[j] with its slice of y and
-//            leaves the partial in shared memory;
-//   barrier  cluster barrier, then every CTA sums the CS partials through
-//            distributed shared memory (fixed rank order, so all CTAs agree)
+//   phase 1  each CTA dots its column slice of W^1[j] with its slice of y
+//            (every load of a warp's batch of rows issued before any use) and
+//            pushes the partial into every peer's shared memory;
+//   barrier  one cluster barrier per sub-chunk, after which every CTA sums
+//            the CS partials locally in a fixed rank order (all CTAs agree)
 //            and applies ReLU (and the row's membership mask when B > 1);
 //   phase 2  each CTA accumulates a_j * W^2[j] over its column slice in
-//            registers; W^2 rows were prefetched into L2 at the start of the
-//            sub-chunk so their HBM reads overlap phase 1 and the barrier.
-// Clusters add their column slices into out with 16-byte fp32 atomics.
-// Selected neurons are processed in sub-chunks of 64 with double-buffered
-// partials, one cluster barrier per sub-chunk.
-
+//            registers; the W^2 rows were prefetched into L2 when the
+//            sub-chunk started and the first loads are in flight across the
+//            barrier.
+// Clusters add their column slices into out with 16-byte fp32 atomics.  The
+// grid holds only as many clusters as fit on the GPU at once (no second
+// wave).  Selected neurons are processed in sub-chunks of 64 with
+// double-buffered partials.
 #include "dv_kernels.h"
 
 namespace dv {
@@ -27,6 +29,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kJS = 64;  // neurons per sub-chunk
+constexpr int kMaxCS = 8;  // largest cluster
 
 struct MlpArgs {
   const void* y;
@@ -42,11 +45,16 @@ struct MlpArgs {
   WsHeader* hdr;
 };
 
-template <typename T, int BT>
-__global__ void __launch_bounds__(kThreads) sparse_mlp_kernel(MlpArgs a) {
+constexpr int kL1 = 12;  // phase-1 loads in flight per lane
+constexpr int kL2 = 10;  // phase-2 loads in flight per thread
+
+// CPLT: 16-byte chunks per lane of a row slice (>= ceil(CPR / 32)).
+template <typename T, int BT, int CPLT>
+__global__ void __launch_bounds__(kThreads, 2) sparse_mlp_kernel(MlpArgs a) {
   constexpr int V = Elem<T>::kVec;
-  extern __shared__ float ys[];  // [BT][w]
-  __shared__ float pd[2][kJS][BT];
+  constexpr int RB = kL1 / CPLT;  // rows per warp per phase-1 batch
+  extern __shared__ float ys[];   // [BT][w]
+  __shared__ float pd[2][kMaxCS][kJS][BT];  // partials pushed by each rank
   __shared__ float as[kJS][BT];
   __shared__ int rows_s[kJS];
 
@@ -57,20 +65,35 @@ __global__ void __launch_bounds__(kThreads) sparse_mlp_kernel(MlpArgs a) {
   const int col0 = rank * w;
   const int nb = min(BT, a.B - a.b0);
 
+  // every CTA of the cluster must be running before a peer stores into its
+  // shared memory: arrive now, wait before the first push
+  cluster_arrive();
+
+  // Batch 1 splits the list by its capacity, so list entries are read in
+  // parallel with the count and the y slice; the batch union splits by the
+  // count.
   int cnt = *a.list_count;
+  const int span = a.member ? max(0, min(cnt, a.cap)) : a.cap;
+  const int n_c = (span + G - 1) / G;
+  const int j_begin = min(span, g * n_c), j_end = min(span, j_begin + n_c);
+  const int row_pre = tid < min(kJS, j_end - j_begin) ? a.list[j_begin + tid] : -1;
+
+  // stage this CTA's slice of y (fp32), 16-byte loads
+  for (int e = tid; e < BT * CPR; e += kThreads) {
+    const int b = e / CPR, c = e - b * CPR;
+    float f[V];
+    if (b < nb) {
+      unpack<T>(ld_cached(static_cast<const T*>(a.y) + (size_t)(a.b0 + b) * a.d + col0 + (size_t)c * V), f);
+    } else {
+#pragma unroll
+      for (int v = 0; v < V; ++v) f[v] = 0.f;
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) ys[b * w + c * V + v] = f[v];
+  }
   if (cnt > a.cap) {
     if (tid == 0 && rank == 0 && g == 0) set_error(a.hdr, DV_ERR_CAPACITY, cnt);
     cnt = a.cap;
-  }
-  cnt = max(cnt, 0);
-  const int n_c = (cnt + G - 1) / G;
-  const int j_begin = min(cnt, g * n_c), j_end = min(cnt, j_begin + n_c);
-
-  // stage this CTA's slice of y (fp32)
-  for (int e = tid; e < BT * w; e += kThreads) {
-    const int b = e / w, c = e - b * w;
-    ys[e] = (b < nb) ? Elem<T>::to_f(static_cast<const T*>(a.y)[(size_t)(a.b0 + b) * a.d + col0 + c])
-                     : 0.f;
   }
 
   const T* W1 = static_cast<const T*>(a.W1n);
@@ -84,14 +107,18 @@ __global__ void __launch_bounds__(kThreads) sparse_mlp_kernel(MlpArgs a) {
     for (int v = 0; v < V; ++v) acc2[b][v] = 0.f;
 
   const int nsub = (j_end - j_begin + kJS - 1) / kJS;
+  cluster_wait();
   for (int sc = 0; sc < nsub; ++sc) {
     const int jj0 = j_begin + sc * kJS;
     const int jn = min(kJS, j_end - jj0);
     const int buf = sc & 1;
     __syncthreads();  // previous sub-chunk done with rows_s / as; ys staged
     if (tid < jn) {
-      int row = a.list[jj0 + tid];
-      if (row < 0 || row >= a.N) {
+      const int j = jj0 + tid;
+      int row = sc == 0 ? row_pre : a.list[j];
+      if (j >= cnt) {
+        row = -1;
+      } else if (row < 0 || row >= a.N) {
         if (rank == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, row);
         row = -1;
       } else {
@@ -101,47 +128,66 @@ __global__ void __launch_bounds__(kThreads) sparse_mlp_kernel(MlpArgs a) {
     }
     __syncthreads();
 
-    // phase 1: partial dot products over this CTA's column slice; a lane
-    // issues all of its (<= 8) 16-byte loads of a row before using them
-    for (int jj = wid; jj < jn; jj += kThreads / 32) {
-      const int row = rows_s[jj];
-      float acc[BT];
+    // phase 1: partial dots over this CTA's column slice; a warp issues all
+    // loads of a batch of RB rows before using them
+    for (int rb0 = wid; rb0 < jn; rb0 += 8 * RB) {
+      uint4 wv[RB][CPLT];
 #pragma unroll
-      for (int b = 0; b < BT; ++b) acc[b] = 0.f;
-      if (row >= 0) {
-        const T* wr = W1 + (size_t)row * a.d + col0;
-        uint4 wv[8];
+      for (int r = 0; r < RB; ++r) {
+        const int jj = rb0 + 8 * r;
+        const int row = jj < jn ? rows_s[jj] : -1;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = lane + 32 * u;
-          if (c < CPR) wv[u] = ld_stream(wr + (size_t)c * V);
+        for (int c = 0; c < CPLT; ++c) {
+          const int ch = lane + 32 * c;
+          if (row >= 0 && ch < CPR) wv[r][c] = ld_stream(W1 + (size_t)row * a.d + col0 + (size_t)ch * V);
         }
+      }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = lane + 32 * u;
-          if (c < CPR) {
-            float wf[V];
-            unpack<T>(wv[u], wf);
+      for (int r = 0; r < RB; ++r) {
+        const int jj = rb0 + 8 * r;
+        if (jj >= jn) break;
+        const int row = rows_s[jj];
+        float acc[BT];
 #pragma unroll
-            for (int b = 0; b < BT; ++b) {
-              const float4* yb = reinterpret_cast<const float4*>(ys + b * w + c * V);
+        for (int b = 0; b < BT; ++b) acc[b] = 0.f;
+        if (row >= 0) {
 #pragma unroll
-              for (int v4 = 0; v4 < V / 4; ++v4) {
-                const float4 yv = yb[v4];
-                acc[b] = fmaf(wf[4 * v4 + 0], yv.x, acc[b]);
-                acc[b] = fmaf(wf[4 * v4 + 1], yv.y, acc[b]);
-                acc[b] = fmaf(wf[4 * v4 + 2], yv.z, acc[b]);
-                acc[b] = fmaf(wf[4 * v4 + 3], yv.w, acc[b]);
+          for (int c = 0; c < CPLT; ++c) {
+            const int ch = lane + 32 * c;
+            if (ch < CPR) {
+              float wf[V];
+              unpack<T>(wv[r][c], wf);
+#pragma unroll
+              for (int b = 0; b < BT; ++b) {
+                const float4* yb = reinterpret_cast<const float4*>(ys + b * w + ch * V);
+#pragma unroll
+                for (int v4 = 0; v4 < V / 4; ++v4) {
+                  const float4 yv = yb[v4];
+                  acc[b] = fmaf(wf[4 * v4 + 0], yv.x, acc[b]);
+                  acc[b] = fmaf(wf[4 * v4 + 1], yv.y, acc[b]);
+                  acc[b] = fmaf(wf[4 * v4 + 2], yv.z, acc[b]);
+                  acc[b] = fmaf(wf[4 * v4 + 3], yv.w, acc[b]);
+                }
               }
             }
           }
         }
-      }
 #pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        const float s = warp_sum(acc[b]);
-        if (lane == 0) pd[buf][jj][b] = s;
+        for (int b = 0; b < BT; ++b) {
+          const float sm = warp_sum(acc[b]);  // every lane holds the sum
+          if (lane < CS) st_dsmem_f32(&pd[buf][rank][jj][b], (uint32_t)lane, sm);
+        }
       }
+    }
+
+    // first batch of phase-2 loads, in flight across the cluster barrier
+    uint4 w2[kL2];
+    const int q_end = gi < NG ? (jn - gi + NG - 1) / NG : 0;  // rows gi, gi + NG, ...
+#pragma unroll
+    for (int q = 0; q < kL2; ++q) {
+      const int jj = gi + q * NG;
+      if (q < q_end && rows_s[jj] >= 0)
+        w2[q] = ld_stream(W2 + (size_t)rows_s[jj] * a.d + col0 + (size_t)cc * V);
     }
     cluster_arrive();
     cluster_wait();
@@ -150,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) sparse_mlp_kernel(MlpArgs a) {
     for (int e = tid; e < jn * BT; e += kThreads) {
       const int jj = e / BT, b = e - jj * BT;
       float sum = 0.f;
-      for (int q = 0; q < CS; ++q) sum += ld_dsmem_f32(&pd[buf][jj][b], (uint32_t)q);
+      for (int q = 0; q < CS; ++q) sum += pd[buf][q][jj][b];
       float act = fmaxf(sum, 0.f);
       const int row = rows_s[jj];
       if (row < 0 || b >= nb) act = 0.f;
@@ -159,36 +205,34 @@ __global__ void __launch_bounds__(kThreads) sparse_mlp_kernel(MlpArgs a) {
     }
     __syncthreads();
 
-    // phase 2: out slice += a_j * W^2[j] (slice), four rows in flight
-    if (gi < NG) {
-      for (int jj = gi; jj < jn; jj += 4 * NG) {
-        uint4 wv[4];
+    // phase 2: out slice += a_j * W^2[j] (slice)
+    for (int q0 = 0; q0 < q_end; q0 += kL2) {
+      if (q0 > 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = jj + u * NG;
-          if (j < jn && rows_s[j] >= 0)
-            wv[u] = ld_stream(W2 + (size_t)rows_s[j] * a.d + col0 + (size_t)cc * V);
+        for (int q = 0; q < kL2; ++q) {
+          const int jj = gi + (q0 + q) * NG;
+          if (q0 + q < q_end && rows_s[jj] >= 0)
+            w2[q] = ld_stream(W2 + (size_t)rows_s[jj] * a.d + col0 + (size_t)cc * V);
         }
+      }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = jj + u * NG;
-          if (j < jn && rows_s[j] >= 0) {
-            float wf[V];
-            unpack<T>(wv[u], wf);
+      for (int q = 0; q < kL2; ++q) {
+        const int jj = gi + (q0 + q) * NG;
+        if (q0 + q < q_end && rows_s[jj] >= 0) {
+          float wf[V];
+          unpack<T>(w2[q], wf);
 #pragma unroll
-            for (int b = 0; b < BT; ++b) {
-              const float ab = as[j][b];
+          for (int b = 0; b < BT; ++b) {
+            const float ab = as[jj][b];
 #pragma unroll
-              for (int v = 0; v < V; ++v) acc2[b][v] = fmaf(ab, wf[v], acc2[b][v]);
-            }
+            for (int v = 0; v < V; ++v) acc2[b][v] = fmaf(ab, wf[v], acc2[b][v]);
           }
         }
       }
     }
   }
-  // no CTA may leave while a peer can still read its partials
-  cluster_arrive();
-  cluster_wait();
+  // No final cluster barrier: peers write into this CTA's shared memory only
+  // before the barrier of the same sub-chunk, which this CTA has passed.
 
   if (gi < NG && j_end > j_begin) {
 #pragma unroll
@@ -271,27 +315,21 @@ ClusterPlan plan_cluster(int chunks) {
   return best;
 }
 
-template <typename T, int BT>
+template <typename T, int BT, int CPLT>
 cudaError_t run_mlp(MlpArgs a, int num_sms, cudaStream_t stream) {
   const size_t smem = (size_t)BT * a.CPR * Elem<T>::kVec * sizeof(float);
-  static int attr_set_for = -1;
-  if (attr_set_for != 1) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_mlp_kernel<T, BT>,
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_mlp_kernel<T, BT, CPLT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(BT * 256 * Elem<T>::kVec * sizeof(float)));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sparse_mlp_kernel<T, BT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(sparse_mlp_kernel<T, BT, CPLT>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    attr_set_for = 1;
+    attr_set = true;
   }
-  // Two CTAs per SM; never more clusters than 64-neuron sub-chunks of work.
-  int G = (2 * num_sms) / a.CS;
-  const int by_work = (a.cap + 15) / 16;
-  G = G < by_work ? G : by_work;
-  G = G < 1 ? 1 : G;
-
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(G * a.CS);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -302,7 +340,32 @@ cudaError_t run_mlp(MlpArgs a, int num_sms, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sparse_mlp_kernel<T, BT>, a);
+  // As many clusters as are co-resident (cached per cluster size and shared
+  // memory), never more than 16-neuron shares of the work.
+  static int cached_cs[kMaxCS + 1] = {0};
+  static size_t cached_smem[kMaxCS + 1] = {0};
+  if (cached_cs[a.CS] == 0 || cached_smem[a.CS] != smem) {
+    cfg.gridDim = dim3(a.CS * num_sms);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mlp_kernel<T, BT, CPLT>, &cfg) != cudaSuccess || n < 1)
+      n = (2 * num_sms) / a.CS;
+    cached_cs[a.CS] = n;
+    cached_smem[a.CS] = smem;
+  }
+  int G = cached_cs[a.CS];
+  const int by_work = (a.cap + 15) / 16;
+  G = G < by_work ? G : by_work;
+  G = G < 1 ? 1 : G;
+  cfg.gridDim = dim3(G * a.CS);
+  return cudaLaunchKernelEx(&cfg, sparse_mlp_kernel<T, BT, CPLT>, a);
+}
+
+template <typename T, int BT>
+cudaError_t run_mlp_cpl(MlpArgs a, int num_sms, cudaStream_t stream) {
+  const int cpl = (a.CPR + 31) / 32;
+  if (cpl <= 2) return run_mlp<T, BT, 2>(a, num_sms, stream);
+  if (cpl <= 4) return run_mlp<T, BT, 4>(a, num_sms, stream);
+  return run_mlp<T, BT, 8>(a, num_sms, stream);
 }
 
 template <typename T>
@@ -326,10 +389,10 @@ cudaError_t mlp_t(const MlpLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t s
     a.b0 = b0;
     cudaError_t e;
     switch (bt) {
-      case 8: e = run_mlp<T, 8>(a, num_sms, stream); break;
-      case 4: e = run_mlp<T, 4>(a, num_sms, stream); break;
-      case 2: e = run_mlp<T, 2>(a, num_sms, stream); break;
-      default: e = run_mlp<T, 1>(a, num_sms, stream); break;
+      case 8: e = run_mlp_cpl<T, 8>(a, num_sms, stream); break;
+      case 4: e = run_mlp_cpl<T, 4>(a, num_sms, stream); break;
+      case 2: e = run_mlp_cpl<T, 2>(a, num_sms, stream); break;
+      default: e = run_mlp_cpl<T, 1>(a, num_sms, stream); break;
     }
     if (e != cudaSuccess) return e;
     b0 += bt;

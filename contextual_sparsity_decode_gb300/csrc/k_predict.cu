@@ -2,13 +2,17 @@
 // threshold selection.  Follows "用Deja Vu来提高 LLM 的推理速度" §2 (稀疏性预测)
 // and the Deja Vu reading notes, "Sparsity operator for MLP / Attention".
 //
-// Launch 1 (predict_gemv<ReLU>):    h = ReLU(y P1)       both predictors
-// Launch 2 (predict_gemv<Sigmoid>): s = sigmoid(h P2)    both predictors
-// Launch 3 (select_kernel):         index lists, one CTA per (predictor, row)
+// Launch 1 (rows_dot<ReLU>):    h = ReLU(y P1)       both predictors
+// Launch 2 (rows_dot<Sigmoid>): s = sigmoid(h P2)    both predictors
+// Launch 3 (select_kernel):     index lists, one CTA per (predictor, row)
 //
-// Both GEMVs are HBM-bound row streams: one warp per weight row, 16-byte
-// read-only loads, four loads in flight per lane, fp32 accumulation and a
-// shuffle reduction.  h and s stay fp32.
+// Both GEMVs are HBM-bound row streams.  A CTA owns a tile of rows; a group
+// of TPR threads (32..256) shares one row, each thread holding up to kC
+// 16-byte chunks of up to kR rows.  Every weight load of a thread is issued
+// before the first one is used, so a CTA keeps kR x kC x 16 B per thread in
+// flight (the probe of this design on GB300: ~1.9 us + bytes / 7.1 TB/s per
+// launch inside a graph).  Reductions run in a fixed order, so scores are
+// reproducible run to run.  h and s stay fp32.
 
 #include "dv_kernels.h"
 
@@ -17,82 +21,112 @@ namespace {
 
 enum Epi { kRelu = 0, kSigmoid = 1 };
 
-struct GemvSeg {
+constexpr int kThreads = 256;
+constexpr int kC = 4;   // chunks per thread per pass
+constexpr int kR = 3;   // rows per thread group
+
+struct RowSeg {
   const void* W;   // [rows][K], storage type T
   const void* x;   // [B][K], XT
   float* out;      // [B][rows]
   int rows, K;
+  int tpr_log2;    // threads per row (log2)
+  int cta0;        // first CTA of the segment
 };
-struct GemvArgs {
-  GemvSeg seg[2];
+struct RowArgs {
+  RowSeg seg[2];
   int nseg;
-  int total_rows;
-  int B;
+  int B, b0;
 };
 
+// Threads per row: the smallest power of two in [32, 256] covering the row's
+// chunks in one pass of kC chunks per thread (256 when none does).
+int tpr_log2_for(int chunks) {
+  int l = 5;
+  while (l < 8 && (1 << l) * kC < chunks) ++l;
+  return l;
+}
+int rows_per_cta(int tpr_log2) { return (kThreads >> tpr_log2) * kR; }
+
 template <typename T, typename XT, int EPI, int BT>
-__global__ void __launch_bounds__(256) predict_gemv(GemvArgs a, int b0) {
+__global__ void __launch_bounds__(kThreads) rows_dot(RowArgs a) {
   constexpr int V = Elem<T>::kVec;
-  constexpr int U = 4;
-  const int lane = threadIdx.x & 31;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  for (int gr = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < a.total_rows;
-       gr += warps_total) {
-    // pick the segment with selects (no dynamic indexing of the parameter block)
-    const bool s1 = a.nseg > 1 && gr >= a.seg[0].rows;
-    const int K = s1 ? a.seg[1].K : a.seg[0].K;
-    const int rows = s1 ? a.seg[1].rows : a.seg[0].rows;
-    const void* Wp = s1 ? a.seg[1].W : a.seg[0].W;
-    const void* xp = s1 ? a.seg[1].x : a.seg[0].x;
-    float* outp = s1 ? a.seg[1].out : a.seg[0].out;
-    const int row = gr - (s1 ? a.seg[0].rows : 0);
-    const int C = K / V;
-    const T* wrow = static_cast<const T*>(Wp) + (size_t)row * K;
-    const XT* xb = static_cast<const XT*>(xp) + (size_t)b0 * K;
-    float acc[BT];
+  __shared__ float red[kThreads / 32][kR][BT];
+  // segment fields picked with selects (no dynamic indexing of the parameter block)
+  const bool s1 = a.nseg > 1 && (int)blockIdx.x >= a.seg[1].cta0;
+  const T* W = static_cast<const T*>(s1 ? a.seg[1].W : a.seg[0].W);
+  const XT* x = static_cast<const XT*>(s1 ? a.seg[1].x : a.seg[0].x);
+  float* out = s1 ? a.seg[1].out : a.seg[0].out;
+  const int rows = s1 ? a.seg[1].rows : a.seg[0].rows;
+  const int K = s1 ? a.seg[1].K : a.seg[0].K;
+  const int tl = s1 ? a.seg[1].tpr_log2 : a.seg[0].tpr_log2;
+  const int cta = (int)blockIdx.x - (s1 ? a.seg[1].cta0 : 0);
+
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tpr = 1 << tl, RS = kThreads >> tl;
+  const int slot = tid >> tl, tt = tid & (tpr - 1);
+  const int row0 = (cta * RS + slot) * kR;
+  const int C = K / V;
+  const int nb = min(BT, a.B - a.b0);
+
+  float acc[kR][BT];
 #pragma unroll
-    for (int b = 0; b < BT; ++b) acc[b] = 0.f;
-    const int nb = min(BT, a.B - b0);
-    for (int c0 = lane; c0 < C; c0 += 32 * U) {
-      uint4 w[U];
+  for (int k = 0; k < kR; ++k)
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u;
-        if (c < C) w[u] = ld_stream(wrow + (size_t)c * V);
+    for (int b = 0; b < BT; ++b) acc[k][b] = 0.f;
+
+  for (int cb = 0; cb < C; cb += tpr * kC) {
+    uint4 w[kR][kC];
+#pragma unroll
+    for (int k = 0; k < kR; ++k)
+#pragma unroll
+      for (int j = 0; j < kC; ++j) {
+        const int c = cb + tt + j * tpr;
+        if (row0 + k < rows && c < C) w[k][j] = ld_stream(W + (size_t)(row0 + k) * K + (size_t)c * V);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u;
-        if (c < C) {
+    for (int j = 0; j < kC; ++j) {
+      const int c = cb + tt + j * tpr;
+      if (c >= C) break;
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        if (b >= nb) break;
+        float xf[V];
+        const XT* xr = x + (size_t)(a.b0 + b) * K + (size_t)c * V;
+        if constexpr (sizeof(XT) == sizeof(T)) {
+          unpack<T>(ld_cached(xr), xf);
+        } else {  // fp32 activations against 16-bit weights: 2 x 16 B
+          unpack<float>(ld_cached(xr), xf);
+          unpack<float>(ld_cached(xr + 4), xf + 4);
+        }
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+          if (row0 + k >= rows) break;
           float wf[V];
-          unpack<T>(w[u], wf);
+          unpack<T>(w[k][j], wf);
 #pragma unroll
-          for (int b = 0; b < BT; ++b) {
-            if (b < nb) {
-              float xf[V];
-              const XT* xr = xb + (size_t)b * K + (size_t)c * V;
-              if constexpr (sizeof(XT) == sizeof(T)) {
-                unpack<T>(ld_cached(xr), xf);
-              } else {  // fp32 activations against 16-bit weights: 2 x 16 B
-                const uint4 lo = ld_cached(xr), hi = ld_cached(xr + 4);
-                unpack<float>(lo, xf);
-                unpack<float>(hi, xf + 4);
-              }
-#pragma unroll
-              for (int v = 0; v < V; ++v) acc[b] = fmaf(wf[v], xf[v], acc[b]);
-            }
-          }
+          for (int v = 0; v < V; ++v) acc[k][b] = fmaf(wf[v], xf[v], acc[k][b]);
         }
       }
     }
+  }
+#pragma unroll
+  for (int k = 0; k < kR; ++k)
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
-      float z = warp_sum(acc[b]);
-      if (lane == 0 && b < nb) {
-        float o = (EPI == kRelu) ? fmaxf(z, 0.f) : 1.f / (1.f + expf(-z));
-        outp[(size_t)(b0 + b) * rows + row] = o;
-      }
+      const float z = warp_sum(acc[k][b]);
+      if (lane == 0) red[wid][k][b] = z;
     }
+  __syncthreads();
+  const int nw = tpr >> 5;  // warps per row group
+  for (int e = tid; e < RS * kR * BT; e += kThreads) {
+    const int sl = e / (kR * BT), k = (e / BT) % kR, b = e % BT;
+    const int row = (cta * RS + sl) * kR + k;
+    if (row >= rows || b >= nb) continue;
+    float z = 0.f;
+    for (int q = 0; q < nw; ++q) z += red[sl * nw + q][k][b];
+    const float o = (EPI == kRelu) ? fmaxf(z, 0.f) : 1.f / (1.f + expf(-z));
+    out[(size_t)(a.b0 + b) * rows + row] = o;
   }
 }
 
@@ -108,26 +142,29 @@ struct SelArgs {
 };
 
 constexpr int kSelThreads = 1024;
-
-// Add 1 to hist[bin] for every active lane, one shared-memory atomic per
-// distinct bin in the warp (scores cluster in few bins of the top digits).
-__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool act) {
-  const uint32_t key = act ? bin : 0xffffffffu;
-  const unsigned grp = __match_any_sync(0xffffffffu, key);
-  const int lane = threadIdx.x & 31;
-  if (act && lane == __ffs(grp) - 1) atomicAdd(&hist[bin], __popc(grp));
-}
+constexpr int kBins = 4096;  // histogram bins per refinement level (12 bits)
+constexpr int kSelLoads = 16;  // score loads in flight per thread
 
 // One CTA per (predictor, batch row).  The row's scores are staged in shared
-// memory; thread t owns the contiguous element range [t*E, (t+1)*E) with E
-// odd, so a warp's reads of element t*E+e hit 32 distinct banks.  Because
-// ranges are contiguous and in thread order, a block prefix sum of per-thread
-// counts gives every selected element its slot in the ascending output.
+// memory as their IEEE bits (sigmoid outputs are >= 0, so the bits order like
+// the values).
+//
+// Top-k finds the exact k-th largest key T by refining a key range: each level
+// bins the keys inside the current range into <= 4096 equal-width bins
+// (width a power of two), finds the bin holding the k-th largest, and narrows
+// the range to it.  The first level spans [min, max] of the row, so 32-bit
+// keys need at most three levels, and only keys inside the range touch the
+// histogram.  Output: every key > T plus the lowest-index keys equal to T,
+// ascending.  Thread t owns the contiguous element range [t*E, (t+1)*E) with
+// E odd (conflict-free bank access), so a block prefix sum of per-thread
+// counts gives every selected element its output slot.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader* hdr) {
   extern __shared__ uint32_t keys[];
+  __shared__ int hist[kBins];
   __shared__ int tmp[32];
-  __shared__ int hist[256];
-  __shared__ int sel_digit, sel_greater;
+  __shared__ uint32_t rlo[32], rhi[32];
+  __shared__ int sel_bin, sel_above;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int b = blockIdx.x;
   const bool p1 = blockIdx.y != 0;
   const int N = p1 ? a.N[1] : a.N[0];
@@ -138,72 +175,113 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
   int32_t* count = p1 ? a.count[1] : a.count[0];
   const float* s = (p1 ? a.s[1] : a.s[0]) + (size_t)b * N;
   int32_t* out = (p1 ? a.idx[1] : a.idx[0]) + (size_t)b * cap;
-  // Scores are sigmoid outputs in [0, 1]: their IEEE bits order like the values.
-  for (int i = threadIdx.x; i < N; i += kSelThreads) keys[i] = __float_as_uint(s[i]);
+
+  // stage the scores: kSelLoads independent loads per thread per round trip
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int ib = tid; ib < N; ib += kSelThreads * kSelLoads) {
+    float v[kSelLoads];
+#pragma unroll
+    for (int q = 0; q < kSelLoads; ++q) {
+      const int i = ib + q * kSelThreads;
+      v[q] = i < N ? __ldcg(s + i) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kSelLoads; ++q) {
+      const int i = ib + q * kSelThreads;
+      if (i < N) {
+        const uint32_t kv = __float_as_uint(v[q]);
+        keys[i] = kv;
+        lo = min(lo, kv);
+        hi = max(hi, kv);
+      }
+    }
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) { rlo[wid] = lo; rhi[wid] = hi; }
   __syncthreads();
   const int E = ((N + kSelThreads - 1) / kSelThreads) | 1;
-  const int i0 = min(N, threadIdx.x * E);
+  const int i0 = min(N, tid * E);
   const int i1 = min(N, i0 + E);
 
   int total;
   if (mode == DV_THRESHOLD) {
-    const float t = thr;
     int mine = 0;
-    for (int i = i0; i < i1; ++i) mine += __uint_as_float(keys[i]) > t;
+    for (int i = i0; i < i1; ++i) mine += __uint_as_float(keys[i]) > thr;
     const int incl = block_inclusive_scan<kSelThreads>(mine, tmp, &total);
     int o = incl - mine;
     for (int i = i0; i < i1; ++i)
-      if (__uint_as_float(keys[i]) > t) {
+      if (__uint_as_float(keys[i]) > thr) {
         if (o < cap) out[o] = i;
         ++o;
       }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       count[b] = min(total, cap);
       if (total > cap) set_error(hdr, DV_ERR_CAPACITY, total);
     }
     return;
   }
 
-  // top-k
   if (k <= 0 || k >= N) {
     if (k >= N)
-      for (int i = threadIdx.x; i < N; i += kSelThreads) out[i] = i;
-    if (threadIdx.x == 0) count[b] = k >= N ? N : 0;
+      for (int i = tid; i < N; i += kSelThreads) out[i] = i;
+    if (tid == 0) count[b] = k >= N ? N : 0;
     return;
   }
-  // Radix select (most significant digit first, 8-bit digits) of the k-th
-  // largest key T; `remaining` counts how many keys equal to T are taken.
-  uint32_t prefix = 0, pmask = 0;
-  int remaining = k;
+  lo = rlo[lane];
+  hi = rhi[lane];
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+
+  // current range [base, top]; `need` keys are still to be taken from it
+  uint32_t base = lo, top = hi;
+  int need = k;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (threadIdx.x < 256) hist[threadIdx.x] = 0;
+  while (top > base) {
+    const uint32_t span = top - base;
+    const int shift = max(0, 32 - __clz((int)span) - 12);
+    const int nbins = (int)(span >> shift) + 1;
+    for (int j = tid; j < nbins; j += kSelThreads) hist[j] = 0;
     __syncthreads();
-    for (int e = 0; e < E; ++e) {  // E is uniform: warps stay converged for match.any
-      const int i = i0 + e;
-      const uint32_t kv = keys[min(i, N - 1)];
-      hist_add(hist, (kv >> shift) & 255u, i < i1 && (kv & pmask) == prefix);
+    for (int i = tid; i < N; i += kSelThreads) {
+      const uint32_t kv = keys[i];
+      if (kv >= base && kv <= top) atomicAdd(&hist[(kv - base) >> shift], 1);
     }
     __syncthreads();
-    const int v = threadIdx.x < 256 ? hist[255 - threadIdx.x] : 0;
+    // bins from the top: thread t sums bins nbins-1-4t .. nbins-4-4t
+    int v4[4], v = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = nbins - 1 - (4 * tid + q);
+      v4[q] = j >= 0 ? hist[j] : 0;
+      v += v4[q];
+    }
     const int incl = block_inclusive_scan<kSelThreads>(v, tmp, &total);
-    if (threadIdx.x < 256 && incl >= remaining && incl - v < remaining) {
-      sel_digit = 255 - threadIdx.x;
-      sel_greater = incl - v;
+    if (incl >= need && incl - v < need) {
+      int above = incl - v;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (above + v4[q] >= need) {
+          sel_bin = nbins - 1 - (4 * tid + q);
+          sel_above = above;
+          break;
+        }
+        above += v4[q];
+      }
     }
     __syncthreads();
-    remaining -= sel_greater;
-    prefix |= (uint32_t)sel_digit << shift;
-    pmask |= 255u << shift;
-    __syncthreads();
+    need -= sel_above;
+    const uint64_t nb = (uint64_t)base + ((uint64_t)sel_bin << shift);
+    const uint64_t nt = nb + ((1ull << shift) - 1);
+    base = (uint32_t)nb;
+    top = (uint32_t)(nt < (uint64_t)top ? nt : (uint64_t)top);
+    __syncthreads();  // sel_* and hist are rewritten by the next level
   }
-  const uint32_t T = prefix;
+  const uint32_t T = base;
   int gt = 0, eq = 0;
   for (int i = i0; i < i1; ++i) { gt += keys[i] > T; eq += keys[i] == T; }
   const int eq_incl = block_inclusive_scan<kSelThreads>(eq, tmp, &total);
-  const int eq_before = eq_incl - eq;
-  const int take_eq = max(0, min(eq, remaining - eq_before));
+  const int take_eq = max(0, min(eq, need - (eq_incl - eq)));
   const int mine = gt + take_eq;
   const int tk_incl = block_inclusive_scan<kSelThreads>(mine, tmp, &total);
   int o = tk_incl - mine;
@@ -213,22 +291,38 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
     if (keys[i] == T) { take = eq_seen < take_eq; ++eq_seen; }
     if (take) out[o++] = i;
   }
-  if (threadIdx.x == 0) count[b] = k;
+  if (tid == 0) count[b] = k;
 }
 
+template <typename T, typename XT, int EPI, int BT>
+cudaError_t launch_rows(RowArgs a, int grid, cudaStream_t stream) {
+  rows_dot<T, XT, EPI, BT><<<grid, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// One launch per batch tile of up to 8 rows; the two segments' CTAs are laid
+// out back to back.
 template <typename T, typename XT, int EPI>
-cudaError_t run_gemv(const GemvArgs& a, cudaStream_t stream) {
-  const int grid = (a.total_rows + 7) / 8;  // one warp per row, 8 warps per CTA
+cudaError_t run_rows(RowArgs a, cudaStream_t stream) {
+  int grid = 0;
+  for (int i = 0; i < a.nseg; ++i) {
+    RowSeg& s = a.seg[i];
+    s.tpr_log2 = tpr_log2_for(s.K / Elem<T>::kVec);
+    s.cta0 = grid;
+    const int rpc = rows_per_cta(s.tpr_log2);
+    grid += (s.rows + rpc - 1) / rpc;
+  }
   for (int b0 = 0; b0 < a.B;) {
     const int nb = a.B - b0;
     const int bt = nb >= 8 ? 8 : (nb >= 4 ? 4 : (nb >= 2 ? 2 : 1));
+    a.b0 = b0;
+    cudaError_t e;
     switch (bt) {
-      case 8: predict_gemv<T, XT, EPI, 8><<<grid, 256, 0, stream>>>(a, b0); break;
-      case 4: predict_gemv<T, XT, EPI, 4><<<grid, 256, 0, stream>>>(a, b0); break;
-      case 2: predict_gemv<T, XT, EPI, 2><<<grid, 256, 0, stream>>>(a, b0); break;
-      default: predict_gemv<T, XT, EPI, 1><<<grid, 256, 0, stream>>>(a, b0); break;
+      case 8: e = launch_rows<T, XT, EPI, 8>(a, grid, stream); break;
+      case 4: e = launch_rows<T, XT, EPI, 4>(a, grid, stream); break;
+      case 2: e = launch_rows<T, XT, EPI, 2>(a, grid, stream); break;
+      default: e = launch_rows<T, XT, EPI, 1>(a, grid, stream); break;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     b0 += bt;
   }
@@ -238,26 +332,18 @@ cudaError_t run_gemv(const GemvArgs& a, cudaStream_t stream) {
 template <typename T>
 cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_preds,
                       WsHeader* hdr, cudaStream_t stream) {
-  GemvArgs g1{};
+  RowArgs g1{};
   g1.nseg = n_preds;
   g1.B = B;
-  g1.total_rows = 0;
-  for (int i = 0; i < n_preds; ++i) {
-    g1.seg[i] = GemvSeg{p.P1t[i], y, p.h[i], p.r[i], d};
-    g1.total_rows += p.r[i];
-  }
-  cudaError_t e = run_gemv<T, T, kRelu>(g1, stream);
+  for (int i = 0; i < n_preds; ++i) g1.seg[i] = RowSeg{p.P1t[i], y, p.h[i], p.r[i], d, 0, 0};
+  cudaError_t e = run_rows<T, T, kRelu>(g1, stream);
   if (e != cudaSuccess) return e;
 
-  GemvArgs g2{};
+  RowArgs g2{};
   g2.nseg = n_preds;
   g2.B = B;
-  g2.total_rows = 0;
-  for (int i = 0; i < n_preds; ++i) {
-    g2.seg[i] = GemvSeg{p.P2t[i], p.h[i], p.s[i], p.N[i], p.r[i]};
-    g2.total_rows += p.N[i];
-  }
-  e = run_gemv<T, float, kSigmoid>(g2, stream);
+  for (int i = 0; i < n_preds; ++i) g2.seg[i] = RowSeg{p.P2t[i], p.h[i], p.s[i], p.N[i], p.r[i], 0, 0};
+  e = run_rows<T, float, kSigmoid>(g2, stream);
   if (e != cudaSuccess) return e;
 
   SelArgs sa{};

@@ -242,7 +242,10 @@ dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h,
 /* ---------------------------------------------------- decoder-step helpers */
 
 /* y_b = LayerNorm(x_b) without affine terms (eps given), rounded to the
- * storage type: the pre-LN input of each sparse block.  x [B][d] fp32. */
+ * storage type: the pre-LN input of each sparse block (the pages do not state
+ * the normalisation; this is the plain pre-LN reading).  x [B][d] fp32,
+ * 16-byte aligned, d a multiple of 4 and at most 16384; y [B][d] 8-byte
+ * aligned.  Other shapes return DV_ERR_INVALID_ARG. */
 dv_status dv_layernorm(const float* x, int B, int d, float eps,
                        void* y, dv_dtype dt, cudaStream_t stream);
 
