@@ -36,14 +36,6 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 int vec_of(dv_dtype dt) { return dt == DV_F32 ? 4 : 8; }
 bool dtype_ok(dv_dtype dt) { return dt == DV_F32 || dt == DV_F16 || dt == DV_BF16; }
 
-// Largest cluster / slice count (<= 8) splitting d into <= 256 chunks per CTA.
-bool row_splits_ok(int d, dv_dtype dt) {
-  const int chunks = d / vec_of(dt);
-  for (int cs = 1; cs <= 8; ++cs)
-    if (chunks % cs == 0 && chunks / cs <= 256) return true;
-  return false;
-}
-
 // Sequential carving of 256-byte aligned regions out of a workspace.  With a
 // null base it only measures.
 struct Carver {
@@ -83,9 +75,11 @@ struct MlpWs {
   uint32_t* member;
   uint16_t* act_hi;
   uint16_t* act_lo;
+  float* act;
 };
-MlpWs carve_mlp(Carver& c, int B, int N) {
+MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   MlpWs w{};
+  w.act = c.take<float>((size_t)B * (B == 1 ? cap : mlp_union_cap(B, N, cap)));
   w.U = c.take<int32_t>((size_t)N);
   w.U_count = c.take<int32_t>(4);
   w.member = c.take<uint32_t>((size_t)B * ((N + 31) / 32));
@@ -102,21 +96,16 @@ struct AttnWs {
   uint32_t* member;
   int32_t* slot_of;
   float* q;
-  float* part;
-  int* ticket;
   float* H;
 };
 AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
   AttnWs w{};
   const int capU = B == 1 ? cap : h;
-  const int n_chunks = (n_max + kAttnChunk - 1) / kAttnChunk;
   w.U = c.take<int32_t>((size_t)h);
   w.U_count = c.take<int32_t>(4);
   w.member = c.take<uint32_t>((size_t)B * ((h + 31) / 32));
   w.slot_of = c.take<int32_t>((size_t)h);
   w.q = c.take<float>((size_t)B * capU * d_h);
-  w.part = c.take<float>((size_t)B * cap * n_chunks * (d_h + 2));
-  w.ticket = c.take<int>((size_t)B * cap);
   w.H = c.take<float>((size_t)B * capU * d_h);
   return w;
 }
@@ -164,7 +153,6 @@ dv_status check_attn(const void* y, int B, int d, int h, int d_h, const void* Wq
   if (d_h != 64 && d_h != 128) return DV_ERR_UNSUPPORTED;
   if (cap < 1 || cap > h) return DV_ERR_INVALID_ARG;
   if (kv->n_max < 16 || kv->n_max > 65536 || kv->n_max % 16) return DV_ERR_INVALID_ARG;
-  if (!row_splits_ok(d, dt)) return DV_ERR_UNSUPPORTED;
   return DV_OK;
 }
 
@@ -178,7 +166,7 @@ AttnLaunch make_attn(const void* y, int B, int d, int h, int d_h, const void* Wq
   L.pos = pos; L.head_idx = head_idx; L.cap = cap; L.head_count = head_count;
   L.scale = scale; L.out = out; L.accumulate = accumulate ? 1 : 0;
   L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.slot_of = w.slot_of;
-  L.q = w.q; L.part = w.part; L.ticket = w.ticket; L.H = w.H;
+  L.q = w.q; L.H = w.H;
   return L;
 }
 }  // namespace
@@ -285,7 +273,7 @@ dv_status dv_lookahead(const void* y, int B, int d, dv_dtype dt, const dv_predic
 dv_status dv_sparse_mlp_workspace_size(int B, int d, int N, int cap, size_t* bytes) {
   if (!bytes || B < 1 || B > kMaxB || d < 1 || N < 1 || cap < 1) return DV_ERR_INVALID_ARG;
   Carver c(nullptr);
-  carve_mlp(c, B, N);
+  carve_mlp(c, B, N, cap);
   *bytes = c.size();
   return DV_OK;
 }
@@ -301,17 +289,16 @@ dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, con
     return DV_ERR_INVALID_ARG;
   if (B < 1 || B > kMaxB || d < 1 || d % vec_of(dt) || N < 1 || N > 65536 || cap < 1)
     return DV_ERR_INVALID_ARG;
-  if (!row_splits_ok(d, dt)) return DV_ERR_UNSUPPORTED;
   Carver meas(nullptr);
-  carve_mlp(meas, B, N);
+  carve_mlp(meas, B, N, cap);
   if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
   Carver c(ws);
-  MlpWs w = carve_mlp(c, B, N);
+  MlpWs w = carve_mlp(c, B, N, cap);
   MlpLaunch L{};
   L.y = y; L.B = B; L.d = d; L.N = N; L.W1n = W1n; L.W2n = W2n;
   L.idx = idx; L.cap = cap; L.count = count; L.out = out; L.accumulate = accumulate ? 1 : 0;
   L.U = w.U; L.U_count = w.U_count; L.member = w.member;
-  L.act_hi = w.act_hi; L.act_lo = w.act_lo;
+  L.act_hi = w.act_hi; L.act_lo = w.act_lo; L.act = w.act;
   cudaError_t e = launch_sparse_mlp(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);
 }

@@ -45,7 +45,12 @@ struct MlpLaunch {
   // tensor-core path: activations split into two storage-type halves,
   // [32][tc_act_cols(N)] each
   void* act_hi; void* act_lo;
+  // CUDA-core path: fp32 activations [B][cap] (B == 1) or [B][mlp_union_cap]
+  float* act;
 };
+
+// Room for the batch union of B lists of up to `cap` neurons out of N.
+int mlp_union_cap(int B, int N, int cap);
 
 // Batches of at least this many rows use the tcgen05 path (16-bit types).
 constexpr int kTcMinBatch = 8;
@@ -76,18 +81,27 @@ struct AttnLaunch {
   // scratch
   int32_t* U; int32_t* U_count; uint32_t* member; int32_t* slot_of;  // union (B > 1)
   float* q;                   // [B][capU][d_h]
-  float* part;                // [B][cap][n_chunks][d_h + 2]
-  int* ticket;                // [B][cap]
   float* H;                   // [B][capU][d_h]
 };
 
-// Positions per split-KV chunk of the decode kernel.
-constexpr int kAttnChunk = 64;
 
 cudaError_t launch_sparse_attn(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
                                int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_repair(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
                              cudaStream_t stream);
+
+// ---- weighted sum of selected rows, column-sliced (k_rows.cu) -----------------
+
+struct CombineLaunch {
+  const void* W; int d;                  // rows of d elements, storage type
+  const int32_t* units; const int32_t* n_units; int cap_units;
+  int rpu;                               // rows per unit: row = units[u] * rpu + t
+  int n_rows_units;                      // valid units are < n_rows_units
+  const float* coef; size_t coef_stride; // coef[b * coef_stride + u * rpu + t]
+  const uint32_t* member; int words;     // optional: unit must be in row b's set
+  int B; float* out; int accumulate; WsHeader* hdr;
+};
+cudaError_t launch_rows_combine(const CombineLaunch& a, dv_dtype dt, cudaStream_t stream);
 
 // ---- misc (k_misc.cu) --------------------------------------------------------
 

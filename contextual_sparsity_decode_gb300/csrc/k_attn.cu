@@ -11,12 +11,14 @@
 //                token(s) and, for K/V rows, the stored embeddings X[j] of
 //                positions whose K/V were skipped (fused repair, so a repair
 //                costs no extra weight traffic).
-//   attn_decode  split-KV softmax: one CTA per (row, head, 64-position chunk),
-//                every K/V load of a warp issued before the first use, partials
-//                combined by the last CTA of each head (ticket counter, no spin
-//                wait).  Also appends X[pos] and updates the valid flags.
-//   attn_out     out += sum_i H_i W_i^O as a weighted sum of the selected
-//                heads' W^O rows, column-sliced across CTAs, fp32 atomics.
+//   attn_decode  split-KV softmax: one thread-block cluster per (row, head),
+//                each CTA a share of the positions with every K/V load of a
+//                batch issued before the first use; partials are pushed into
+//                rank 0's shared memory and combined after one cluster barrier.
+//                Also appends X[pos] and updates the valid flags.
+//   rows_combine out += sum_i H_i W_i^O as a weighted sum of the selected
+//                heads' W^O rows, column-sliced so every output element has
+//                one writer (k_rows.cu).
 // The standalone repair (dv_kv_repair, e.g. a dense prefill) uses a tiled
 // CUDA-core GEMM over the missing positions instead.
 
@@ -26,8 +28,6 @@ namespace dv {
 namespace {
 
 constexpr int kCur = 1 << 30;      // entry flag: the current token (vector = y_b)
-constexpr int kCH = kAttnChunk;
-constexpr int kMaxChunks = 65536 / kAttnChunk;  // n_max <= 65536
 
 struct AttnArgs {
   const void* y;
@@ -47,11 +47,9 @@ struct AttnArgs {
   const uint32_t* member;   // [B][hwords], nullptr when B == 1
   int hwords;
   const int32_t* slot_of;   // head -> union slot, nullptr when B == 1
-  int B, d, h, d_h, n_max, n_chunks;
+  int B, d, h, d_h, n_max;
   float scale;
   float* q;
-  float* part;
-  int* ticket;
   float* H;
   float* out;
   WsHeader* hdr;
@@ -273,14 +271,33 @@ template <> struct KvRaw<__half, 2> : KvRaw16x2<__half> {};
 template <> struct KvRaw<__nv_bfloat16, 4> : KvRaw16x4<__nv_bfloat16> {};
 template <> struct KvRaw<__nv_bfloat16, 2> : KvRaw16x2<__nv_bfloat16> {};
 
+// One thread-block cluster of CSd CTAs per (row, selected head): CTA `rank`
+// takes a contiguous share of the positions 0..pos, runs the softmax over it
+// in batches of 8 warps x kPW positions (every K/V load of a batch issued
+// before the first use, online max/sum across batches), and pushes its
+// (max, sum, numerator[d_h]) into rank 0's shared memory; after one cluster
+// barrier rank 0 combines the CSd partials in rank order and writes H.
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kMaxCSd = 16;
+
 template <typename T, int DH>
-__global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   constexpr int E = DH / 32;
-  const int c = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+  constexpr int kPW = 16;                              // positions per warp per batch
+  constexpr int kPB = sizeof(T) == 2 ? kPW : kPW / 2;  // loads issued together
+  using Raw = typename KvRaw<T, E>::type;
+  __shared__ float sm[kDecWarps], sl[kDecWarps];
+  __shared__ float sacc[kDecWarps][DH];
+  __shared__ float cm[kMaxCSd], cl[kMaxCSd];
+  __shared__ float cacc[kMaxCSd][DH];
+  const int s = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int CSd = (int)gridDim.x;  // the grid is one cluster wide
+  const int rank = (int)cluster_ctarank();
   const int p = row_pos(a, b);
-  if (s == a.cap) {  // housekeeping of row b: append X[p], reset the valid column
-    if (c != 0) return;
+  if (s == a.cap) {  // housekeeping of row b (rank 0 only): append X[p], reset the valid column
+    if (rank != 0) return;
     if (p < 0) {
       if (tid == 0) set_error(a.hdr, DV_ERR_POSITION, a.pos[b]);
       return;
@@ -288,23 +305,23 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
     constexpr int V = Elem<T>::kVec;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.y) + (size_t)b * a.d);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + ((size_t)b * a.n_max + p) * a.d);
-    for (int k0 = tid; k0 < a.d / V; k0 += 8 * blockDim.x) {  // 8 loads in flight, then 8 stores
+    for (int k0 = tid; k0 < a.d / V; k0 += 8 * kDecThreads) {  // 8 loads in flight, then 8 stores
       uint4 t8[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const int k = k0 + q * blockDim.x;
+        const int k = k0 + q * kDecThreads;
         if (k < a.d / V) t8[q] = __ldg(src + k);
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const int k = k0 + q * blockDim.x;
+        const int k = k0 + q * kDecThreads;
         if (k < a.d / V) dst[k] = t8[q];
       }
     }
-    for (int i = tid; i < a.h; i += blockDim.x) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
+    for (int i = tid; i < a.h; i += kDecThreads) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
     __syncthreads();
     const int cnt = max(0, min(a.head_count[b], a.cap));
-    for (int e = tid; e < cnt; e += blockDim.x) {
+    for (int e = tid; e < cnt; e += kDecThreads) {
       const int i = a.head_idx[(size_t)b * a.cap + e];
       if (i >= 0 && i < a.h) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 1;
     }
@@ -314,81 +331,81 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   const int cnt_raw = a.head_count[b];
   const int i = a.head_idx[(size_t)b * a.cap + s];
   const int cnt = max(0, min(cnt_raw, a.cap));
-  if (s >= cnt || p < 0) return;
+  if (s >= cnt) return;  // the whole cluster agrees
   if (i < 0 || i >= a.h) {
-    if (tid == 0 && c == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
+    if (tid == 0 && rank == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
     return;
   }
   const int u = a.slot_of ? a.slot_of[i] : s;
-  const int n_pos = p + 1;
-  const int nch = (n_pos + kCH - 1) / kCH;
-  if (c >= nch) return;
-  const int j0 = c * kCH, j1 = min(n_pos, j0 + kCH);
+  float* Hrow = a.H + ((size_t)b * a.capU + u) * DH;
+  if (p < 0) {  // nothing to attend: H = 0 (the position error is reported by housekeeping)
+    if (rank == 0)
+      for (int t = tid; t < DH; t += kDecThreads) Hrow[t] = 0.f;
+    return;
+  }
+  cluster_arrive();  // every CTA must be running before peers push into rank 0
 
-  __shared__ float sm[4], sl[4];
-  __shared__ float sacc[4][DH];
-  __shared__ float wts[kMaxChunks];
-  __shared__ int is_last;
+  const int n_pos = p + 1;
+  const int per = (n_pos + CSd - 1) / CSd;
+  const int j_lo = min(n_pos, rank * per), j_hi = min(n_pos, j_lo + per);
 
   float qr[E];
   const float* qg = a.q + ((size_t)b * a.capU + u) * DH + lane * E;
 #pragma unroll
   for (int e = 0; e < E; ++e) qr[e] = qg[e] * a.scale;
-
   const T* Kr = static_cast<const T*>(a.K) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
   const T* Vr = static_cast<const T*>(a.V) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
-  // each warp owns kCH/4 consecutive positions, loaded kPB at a time with
-  // every K and V load of the batch issued before the first use
-  constexpr int kPW = kCH / 4;
-  constexpr int kPB = sizeof(T) == 2 ? kPW : kPW / 2;
-  using Raw = typename KvRaw<T, E>::type;
+
   float mw = -INFINITY, lw = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const int jw = j0 + wid * kPW;
 #pragma unroll 1
-  for (int jb = jw; jb < min(j1, jw + kPW); jb += kPB) {
-    Raw kraw[kPB], vraw[kPB];
+  for (int jw0 = j_lo + wid * kPW; jw0 < j_hi; jw0 += kDecWarps * kPW) {
+    const int jw1 = min(j_hi, jw0 + kPW);
+#pragma unroll 1
+    for (int jb = jw0; jb < jw1; jb += kPB) {
+      Raw kraw[kPB], vraw[kPB];
 #pragma unroll
-    for (int s2 = 0; s2 < kPB; ++s2) {
-      const int j = jb + s2;
-      if (j < j1) {
-        kraw[s2] = KvRaw<T, E>::load(Kr + (size_t)j * DH);
-        vraw[s2] = KvRaw<T, E>::load(Vr + (size_t)j * DH);
+      for (int s2 = 0; s2 < kPB; ++s2) {
+        const int j = jb + s2;
+        if (j < jw1) {
+          kraw[s2] = KvRaw<T, E>::load(Kr + (size_t)j * DH);
+          vraw[s2] = KvRaw<T, E>::load(Vr + (size_t)j * DH);
+        }
       }
-    }
-    float lg[kPB];
-    float mb = -INFINITY;
+      float lg[kPB];
+      float mb = -INFINITY;
 #pragma unroll
-    for (int s2 = 0; s2 < kPB; ++s2) {
-      lg[s2] = -INFINITY;
-      if (jb + s2 < j1) {
-        float kf[E];
-        KvRaw<T, E>::to_f(kraw[s2], kf);
-        float dot = 0.f;
+      for (int s2 = 0; s2 < kPB; ++s2) {
+        lg[s2] = -INFINITY;
+        if (jb + s2 < jw1) {
+          float kf[E];
+          KvRaw<T, E>::to_f(kraw[s2], kf);
+          float dot = 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
-        lg[s2] = warp_sum(dot);
-        mb = fmaxf(mb, lg[s2]);
+          for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
+          lg[s2] = warp_sum(dot);
+          mb = fmaxf(mb, lg[s2]);
+        }
       }
-    }
-    const float mn = fmaxf(mw, mb);
-    const float corr = expf(mw - mn);  // 0 on the first batch (mw = -inf)
-    lw *= corr;
+      const float mn = fmaxf(mw, mb);
+      const float corr = expf(mw - mn);  // 0 on the first batch (mw = -inf)
+      lw *= corr;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] *= corr;
+      for (int e = 0; e < E; ++e) acc[e] *= corr;
 #pragma unroll
-    for (int s2 = 0; s2 < kPB; ++s2) {
-      if (jb + s2 < j1) {
-        const float pj = expf(lg[s2] - mn);
-        float vf[E];
-        KvRaw<T, E>::to_f(vraw[s2], vf);
-        lw += pj;
+      for (int s2 = 0; s2 < kPB; ++s2) {
+        if (jb + s2 < jw1) {
+          const float pj = expf(lg[s2] - mn);
+          float vf[E];
+          KvRaw<T, E>::to_f(vraw[s2], vf);
+          lw += pj;
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
+        }
       }
+      mw = mn;
     }
-    mw = mn;
   }
   if (lane == 0) { sm[wid] = mw; sl[wid] = lw; }
 #pragma unroll
@@ -396,145 +413,39 @@ __global__ void __launch_bounds__(128) attn_decode_kernel(AttnArgs a) {
   __syncthreads();
   float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) M = fmaxf(M, sm[w]);
-  float* prt = a.part + (((size_t)b * a.cap + s) * a.n_chunks + c) * (DH + 2);
-  for (int t = tid; t < DH; t += blockDim.x) {
+  for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm[w]);
+  cluster_wait();
+  // push this CTA's partial into rank 0
+  for (int t = tid; t < DH; t += kDecThreads) {
     float A = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < kDecWarps; ++w)
       if (sm[w] != -INFINITY) A += sacc[w][t] * expf(sm[w] - M);
-    prt[2 + t] = A;
+    st_dsmem_f32(&cacc[rank][t], 0u, A);
   }
   if (tid == 0) {
-    float L = 0.f;
-    for (int w = 0; w < 4; ++w)
-      if (sm[w] != -INFINITY) L += sl[w] * expf(sm[w] - M);
-    prt[0] = M;
-    prt[1] = L;
+    float Lsum = 0.f;
+    for (int w = 0; w < kDecWarps; ++w)
+      if (sm[w] != -INFINITY) Lsum += sl[w] * expf(sm[w] - M);
+    st_dsmem_f32(&cm[rank], 0u, M);
+    st_dsmem_f32(&cl[rank], 0u, Lsum);
   }
-  // every position before p of a selected head is now present (repaired above)
+  // every position before p of a selected head is now present (repaired by attn_qkv)
   uint8_t* vrow = a.valid + ((size_t)b * a.h + i) * a.n_max;
-  for (int j = j0 + tid; j < min(j1, p); j += blockDim.x) vrow[j] = 1;
-
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int old = atomicAdd(&a.ticket[(size_t)b * a.cap + s], 1);
-    is_last = (old == nch - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // combine the chunks: per-chunk weights w_k = exp(M_k - M) in shared memory,
-  // then one pass over the partial numerators with 16 loads in flight
-  const float* pb = a.part + ((size_t)b * a.cap + s) * a.n_chunks * (DH + 2);
-  float mloc = -INFINITY;
-  for (int k = tid; k < nch; k += blockDim.x) mloc = fmaxf(mloc, __ldcg(pb + (size_t)k * (DH + 2)));
-  mloc = warp_max(mloc);
-  if (lane == 0) sm[wid] = mloc;
-  __syncthreads();
-  const float Mg = fmaxf(fmaxf(sm[0], sm[1]), fmaxf(sm[2], sm[3]));
-  float lloc = 0.f;
-  for (int k = tid; k < nch; k += blockDim.x) {
-    const float* pk = pb + (size_t)k * (DH + 2);
-    const float wk = expf(__ldcg(pk) - Mg);
-    wts[k] = wk;
-    lloc += __ldcg(pk + 1) * wk;
-  }
-  lloc = warp_sum(lloc);
-  if (lane == 0) sl[wid] = lloc;
-  __syncthreads();
-  const float den = (sl[0] + sl[1]) + (sl[2] + sl[3]);
-  for (int t = tid; t < DH; t += blockDim.x) {
+  for (int j = j_lo + tid; j < min(j_hi, p); j += kDecThreads) vrow[j] = 1;
+  cluster_arrive();
+  cluster_wait();
+  if (rank != 0) return;
+  float Mg = -INFINITY;
+  for (int r = 0; r < CSd; ++r) Mg = fmaxf(Mg, cm[r]);
+  float den = 0.f;
+  for (int r = 0; r < CSd; ++r)
+    if (cm[r] != -INFINITY) den += cl[r] * expf(cm[r] - Mg);
+  for (int t = tid; t < DH; t += kDecThreads) {
     float num = 0.f;
-#pragma unroll 16
-    for (int k = 0; k < nch; ++k) num += __ldcg(pb + (size_t)k * (DH + 2) + 2 + t) * wts[k];
-    a.H[((size_t)b * a.capU + u) * DH + t] = num / den;
-  }
-  if (tid == 0) a.ticket[(size_t)b * a.cap + s] = 0;
-}
-
-// ---------------------------------------------------------------------------
-// attn_out: out_b += sum_{u, t} H[b][u][t] * Wo[U[u]][t][:]
-
-struct SlicePlan {
-  int CS = 0, CPR = 0;
-};
-SlicePlan plan_slices(int chunks) {
-  SlicePlan best;
-  for (int pass = 0; pass < 2 && best.CS == 0; ++pass)
-    for (int cs = 8; cs >= 1; --cs) {
-      if (chunks % cs) continue;
-      const int cpr = chunks / cs;
-      if (cpr > 256) continue;
-      if (pass == 0 && cpr % 32) continue;
-      best.CS = cs;
-      best.CPR = cpr;
-      break;
-    }
-  return best;
-}
-
-constexpr int kOL = 12;  // W^O row loads in flight per thread
-
-template <typename T, int BT>
-__global__ void __launch_bounds__(256) attn_out_kernel(AttnArgs a, int CS, int CPR, int b0) {
-  constexpr int V = Elem<T>::kVec;
-  const int tid = threadIdx.x;
-  const int slice = blockIdx.x % CS, g = blockIdx.x / CS, G = gridDim.x / CS;
-  const int col0 = slice * CPR * V;
-  const int nb = min(BT, a.B - b0);
-  const int R = union_count(a) * a.d_h;
-  const int rc = (R + G - 1) / G;
-  const int r0 = min(R, g * rc), r1 = min(R, r0 + rc);
-  const int NG = 256 / CPR, cc = tid % CPR, gi = tid / CPR;
-  if (gi >= NG || r0 >= r1) return;
-  const T* Wo = static_cast<const T*>(a.Wo);
-  float acc[BT][V];
-#pragma unroll
-  for (int b = 0; b < BT; ++b)
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[b][v] = 0.f;
-  // every thread issues up to kOL row loads before using any
-  for (int r = r0 + gi; r < r1; r += kOL * NG) {
-    uint4 wv[kOL];
-    int ii[kOL], uu[kOL], tt[kOL];
-#pragma unroll
-    for (int k = 0; k < kOL; ++k) {
-      const int rr = r + k * NG;
-      ii[k] = -1;
-      if (rr < r1) {
-        uu[k] = rr / a.d_h;
-        tt[k] = rr - uu[k] * a.d_h;
-        ii[k] = a.U[uu[k]];
-        if (ii[k] >= 0 && ii[k] < a.h)
-          wv[k] = ld_stream(Wo + ((size_t)ii[k] * a.d_h + tt[k]) * a.d + col0 + (size_t)cc * V);
-        else
-          ii[k] = -1;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kOL; ++k) {
-      if (ii[k] < 0) continue;
-      float wf[V];
-      unpack<T>(wv[k], wf);
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        if (b >= nb) break;
-        const int bb = b0 + b;
-        if (!member_of(a, bb, ii[k]) || row_pos(a, bb) < 0) continue;
-        const float coef = a.H[((size_t)bb * a.capU + uu[k]) * a.d_h + tt[k]];
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[b][v] = fmaf(coef, wf[v], acc[b][v]);
-      }
-    }
-  }
-#pragma unroll
-  for (int b = 0; b < BT; ++b) {
-    if (b >= nb) break;
-    float* o = a.out + (size_t)(b0 + b) * a.d + col0 + (size_t)cc * V;
-#pragma unroll
-    for (int v = 0; v < V; v += 4) atomic_add_f32x4(o + v, acc[b][v], acc[b][v + 1], acc[b][v + 2], acc[b][v + 3]);
+    for (int r = 0; r < CSd; ++r)
+      if (cm[r] != -INFINITY) num += cacc[r][t] * expf(cm[r] - Mg);
+    Hrow[t] = num / den;
   }
 }
 
@@ -670,9 +581,8 @@ AttnArgs make_args(const AttnLaunch& L, WsHeader* hdr) {
   a.K = L.K; a.V = L.V; a.X = L.X; a.valid = L.valid;
   a.pos = L.pos; a.head_idx = L.head_idx; a.head_count = L.head_count; a.cap = L.cap;
   a.B = L.B; a.d = L.d; a.h = L.h; a.d_h = L.d_h; a.n_max = L.n_max;
-  a.n_chunks = (L.n_max + kCH - 1) / kCH;
   a.scale = L.scale;
-  a.q = L.q; a.part = L.part; a.ticket = L.ticket; a.H = L.H;
+  a.q = L.q; a.H = L.H;
   a.out = L.out; a.hdr = hdr;
   a.hwords = (L.h + 31) / 32;
   if (L.B == 1) {
@@ -685,6 +595,60 @@ AttnArgs make_args(const AttnLaunch& L, WsHeader* hdr) {
   return a;
 }
 
+template <typename T> dv_dtype dtype_of();
+template <> dv_dtype dtype_of<float>() { return DV_F32; }
+template <> dv_dtype dtype_of<__half>() { return DV_F16; }
+template <> dv_dtype dtype_of<__nv_bfloat16>() { return DV_BF16; }
+
+// Cluster width of the decode kernel: 16 CTAs where the GPU can hold such
+// clusters (non-portable size), else 8.
+template <typename T, int DH>
+int decode_cluster_width() {
+  static int w = 0;
+  if (w == 0) {
+    w = 8;
+    if (cudaFuncSetAttribute(attn_decode_kernel<T, DH>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(kDecThreads);
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 16;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<T, DH>, &cfg) == cudaSuccess && n >= 1) w = 16;
+    }
+    (void)cudaGetLastError();
+  }
+  return w;
+}
+
+template <typename T, int DH>
+cudaError_t launch_decode_dh(const AttnArgs& a, cudaStream_t stream) {
+  const int cw = decode_cluster_width<T, DH>();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cw, a.cap + 1, a.B);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cw;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, DH>, a);
+}
+
+template <typename T>
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
+  return a.d_h == 128 ? launch_decode_dh<T, 128>(a, stream) : launch_decode_dh<T, 64>(a, stream);
+}
+
 template <typename T>
 cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t stream) {
   AttnArgs a = make_args(L, hdr);
@@ -694,37 +658,17 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   attn_qkv_kernel<T><<<a.capU * RG, 256, 0, stream>>>(a, RG, tl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // 2. split-KV softmax, last-CTA combine, cache bookkeeping
-  dim3 g2(a.n_chunks, a.cap + 1, a.B);
-  if (a.d_h == 128) attn_decode_kernel<T, 128><<<g2, 128, 0, stream>>>(a);
-  else attn_decode_kernel<T, 64><<<g2, 128, 0, stream>>>(a);
-  e = cudaGetLastError();
+  // 2. split-KV softmax, one cluster per (row, head), cache bookkeeping
+  e = launch_decode<T>(a, stream);
   if (e != cudaSuccess) return e;
-  // 3. output projection
-  if (!L.accumulate) {
-    e = cudaMemsetAsync(L.out, 0, (size_t)L.B * L.d * sizeof(float), stream);
-    if (e != cudaSuccess) return e;
-  }
-  const SlicePlan sp = plan_slices(a.d / Elem<T>::kVec);
-  if (sp.CS == 0) return cudaErrorInvalidValue;
-  int G = (2 * num_sms) / sp.CS;
-  const int by_rows = (a.capU * a.d_h + 15) / 16;
-  G = G < by_rows ? G : by_rows;
-  G = G < 1 ? 1 : G;
-  for (int b0 = 0; b0 < a.B;) {
-    const int nb = a.B - b0;
-    const int bt = nb >= 8 ? 8 : (nb >= 4 ? 4 : (nb >= 2 ? 2 : 1));
-    switch (bt) {
-      case 8: attn_out_kernel<T, 8><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
-      case 4: attn_out_kernel<T, 4><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
-      case 2: attn_out_kernel<T, 2><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
-      default: attn_out_kernel<T, 1><<<G * sp.CS, 256, 0, stream>>>(a, sp.CS, sp.CPR, b0); break;
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    b0 += bt;
-  }
-  return cudaSuccess;
+  // 3. output projection: out (+)= sum_u sum_t H[b][u][t] Wo[U[u]][t][:]
+  CombineLaunch c{};
+  c.W = L.Wo; c.d = a.d;
+  c.units = a.U; c.n_units = a.U_count; c.cap_units = a.capU; c.rpu = a.d_h; c.n_rows_units = a.h;
+  c.coef = a.H; c.coef_stride = (size_t)a.capU * a.d_h;
+  c.member = a.member; c.words = a.hwords;
+  c.B = a.B; c.out = L.out; c.accumulate = L.accumulate; c.hdr = hdr;
+  return launch_rows_combine(c, dtype_of<T>(), stream);
 }
 
 template <typename T>

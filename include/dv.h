@@ -142,7 +142,8 @@ dv_status dv_predict_workspace_size(int B, int n_preds, int r_max, int N_max,
  * then top-k or threshold selection into p.idx[b][...] (ascending) and
  * p.count[b].  Top-k ranks by s, ties to the lower index.  1 <= n_preds <= 2;
  * both predictors read the same y [B][d] and run in fused launches.
- * Limits: B <= 32, d <= 16384, r <= 4096, N <= 65536. */
+ * Limits: B <= 32, d <= 16384, r <= 4096, N <= 53248 (the selection stages
+ * one row's scores in shared memory). */
 dv_status dv_predict(const void* y, int B, int d, dv_dtype dt,
                      const dv_predictor* preds, int n_preds,
                      void* ws, size_t ws_bytes, cudaStream_t stream);
