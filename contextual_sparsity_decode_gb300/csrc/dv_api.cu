@@ -151,6 +151,8 @@ dv_status check_attn(const void* y, int B, int d, int h, int d_h, const void* Wq
     return DV_ERR_INVALID_ARG;
   if (B < 1 || B > kMaxB || d < 1 || d % vec_of(dt) || h < 1 || h > 1024) return DV_ERR_INVALID_ARG;
   if (d_h != 64 && d_h != 128) return DV_ERR_UNSUPPORTED;
+  // one projection row must fit a 40 KB shared-memory stage of attn_qkv
+  if ((size_t)d * (dt == DV_F32 ? 4 : 2) > 40960) return DV_ERR_UNSUPPORTED;
   if (cap < 1 || cap > h) return DV_ERR_INVALID_ARG;
   if (kv->n_max < 16 || kv->n_max > 65536 || kv->n_max % 16) return DV_ERR_INVALID_ARG;
   return DV_OK;

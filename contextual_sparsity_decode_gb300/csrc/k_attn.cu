@@ -79,7 +79,7 @@ __device__ __forceinline__ int row_pos(const AttnArgs& a, int b) {
 
 constexpr int kQC = 4;      // chunks per thread per pass over a row
 constexpr int kQR = 4;      // rows per thread group (divides d_h)
-constexpr int kNE = 4;      // vectors per group of entries
+constexpr int kNE = 2;      // vectors per group of entries
 constexpr int kWin = 4096;  // positions scanned per repair window (256 x 16)
 
 int qkv_tpr_log2(int chunks) {
@@ -106,7 +106,7 @@ __device__ __forceinline__ void qkv_load_w(const T* wbase, int d, int C, int cb,
 template <typename T>
 __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)[kQR][kQC],
                             bool one_pass, const T* wbase, int tl, int m, int tbase, int i, int u,
-                            float (&red)[8][kQR][kNE]) {
+                            float (&red)[8][kQR][kNE], const uint4 (&ycur)[kQC], bool ycur_ok) {
   constexpr int V = Elem<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int tpr = 1 << tl, RS = 256 >> tl, tt = tid & (tpr - 1);
@@ -133,7 +133,8 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
           const int b = (en >> 20) & 1023, jp = en & 0xfffff;
           const T* vec = (en & kCur) ? y + (size_t)b * a.d : X + ((size_t)b * a.n_max + jp) * a.d;
           float xf[V];
-          unpack<T>(ld_cached(vec + (size_t)c * V), xf);
+          if ((en & kCur) && ycur_ok) unpack<T>(ycur[j], xf);  // preloaded (batch 1, one pass)
+          else unpack<T>(ld_cached(vec + (size_t)c * V), xf);
 #pragma unroll
           for (int k = 0; k < kQR; ++k) {
             float wf[V];
@@ -182,21 +183,38 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   const int tpr = 1 << tl, RS = 256 >> tl, slot = tid >> tl, tt = tid & (tpr - 1);
   const int rpc = RS * kQR;
   const int u = blockIdx.x / RG, rg = blockIdx.x % RG;
-  const int i = a.U[u];  // u < capU: in bounds; loaded together with the count
+  const int r0 = rg * rpc;        // first row of the CTA within the head's 3 d_h rows
+  const int m = r0 / a.d_h;       // 0 = Q, 1 = K, 2 = V
+  const int tbase = r0 - m * a.d_h;
+  const int C = a.d / V;
+  const bool one_pass = C <= tpr * kQC;
+  // round trip 1: head index (u < capU keeps it in bounds), count, position
+  // and (batch 1) this thread's chunks of the current token
+  const int i = a.U[u];
+  const int p0 = a.B == 1 ? row_pos(a, 0) : -1;
+  const bool ycur_ok = a.B == 1 && one_pass;
+  uint4 ycur[kQC];
+  if (ycur_ok) {
+#pragma unroll
+    for (int j = 0; j < kQC; ++j) {
+      const int c = tt + j * tpr;
+      if (c < C) ycur[j] = ld_cached(static_cast<const T*>(a.y) + (size_t)c * V);
+    }
+  }
   if (u >= union_count(a)) return;
   if (i < 0 || i >= a.h) {
     if (tid == 0 && rg == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
     return;
   }
-  const int r0 = rg * rpc;        // first row of the CTA within the head's 3 d_h rows
-  const int m = r0 / a.d_h;       // 0 = Q, 1 = K, 2 = V
-  const int tbase = r0 - m * a.d_h;
+  // round trip 2: the weights and (batch 1, K/V rows) the valid flags
   const T* wbase = static_cast<const T*>(a.Wqkv) +
                    ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
-  const int C = a.d / V;
-  const bool one_pass = C <= tpr * kQC;
   uint4 w[kQR][kQC];
   if (one_pass) qkv_load_w<T>(wbase, a.d, C, 0, tt, tpr, w);
+  const bool fast_scan = a.B == 1 && m > 0 && p0 >= 0 && p0 <= kWin;
+  uint4 vflags = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+  if (fast_scan && tid * 16 < p0)
+    vflags = *reinterpret_cast<const uint4*>(a.valid + (size_t)i * a.n_max + tid * 16);
 
   if (tid == 0) n_ent = 0;
   __syncthreads();
@@ -205,7 +223,7 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
     if (p >= 0 && member_of(a, b, i)) ent[atomicAdd(&n_ent, 1)] = kCur | (b << 20) | p;
   }
   __syncthreads();
-  qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red);
+  qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok);
   if (m == 0) return;
   // K/V rows: positions whose K/V were skipped, one window of 4096 at a time
   for (int b = 0; b < a.B; ++b) {
@@ -213,21 +231,25 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
     if (p < 0 || !member_of(a, b, i)) continue;
     const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
     for (int base = 0; base < p; base += kWin) {
+      const int j0 = base + tid * 16;
+      const uint4 v4 = fast_scan ? vflags
+                       : (j0 < p ? *reinterpret_cast<const uint4*>(vr + j0)
+                                 : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu));
+      const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+      int mine = 0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        mine += (j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0);
+      if (!__syncthreads_or(mine)) continue;  // nothing to repair in this window
       if (tid == 0) n_ent = 0;
       __syncthreads();
-      const int j0 = base + tid * 16;
-      if (j0 < p) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(vr + j0);
-        const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int j = j0 + k;
-          if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0)
-            ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
-        }
+      for (int k = 0; k < 16; ++k) {
+        const int j = j0 + k;
+        if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0) ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
       }
       __syncthreads();
-      qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red);
+      qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false);
     }
   }
 }

@@ -7,9 +7,10 @@
 //
 // A CTA owns kCW 16-byte column chunks of out and walks every selected row,
 // so each output element is produced by exactly one CTA: no atomics, and the
-// summation order is fixed.  Threads split the rows (NRG row groups x kCW
-// chunks); each issues kPL row loads before using any.  The partial sums are
-// reduced across lanes with shuffles and across warps in shared memory.
+// summation order is fixed.  Memory round trips are the cost that matters,
+// so a batch of rows takes two: the unit ids (staged in shared memory) and
+// the thread's coefficients are loaded together, then all kPL row loads of
+// the thread are issued before any is used.
 
 #include "dv_kernels.h"
 
@@ -19,13 +20,14 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kCW = 4;                   // 16-byte column chunks per CTA
 constexpr int kNRG = kThreads / kCW;     // row groups
-constexpr int kPL = 16;                  // row loads in flight per thread
+constexpr int kPL = 16;                  // rows per thread per batch
+constexpr int kUnitsMax = 1024;          // unit ids staged per batch
 
 template <typename T, int BT>
 __global__ void __launch_bounds__(kThreads) rows_combine_kernel(CombineLaunch a, int b0) {
   constexpr int V = Elem<T>::kVec;
   __shared__ float red[kThreads / 32][kCW][BT][V];
-  __shared__ int unit_s[1024];
+  __shared__ int unit_s[kUnitsMax];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int c = tid % kCW, rg = tid / kCW;
   const int C = a.d / V;
@@ -41,54 +43,56 @@ __global__ void __launch_bounds__(kThreads) rows_combine_kernel(CombineLaunch a,
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[b][v] = 0.f;
 
-  // units staged in shared memory, 1024 at a time
-  for (int ub = 0; ub < n_units; ub += 1024) {
-    const int un = min(1024, n_units - ub);
-    __syncthreads();
-    for (int e = tid; e < un; e += kThreads) {
-      int j = a.units[ub + e];
+  // a batch covers kPL * kNRG rows and at most kUnitsMax units
+  const int rows_per_batch = min(kPL * kNRG, kUnitsMax * a.rpu);
+  for (int rb = 0; rb < R; rb += rows_per_batch) {
+    const int re = min(R, rb + rows_per_batch);
+    const int u0 = rb / a.rpu, u1 = (re - 1) / a.rpu + 1;
+    __syncthreads();  // unit_s of the previous batch is no longer read
+    for (int e = tid; e < u1 - u0; e += kThreads) {
+      int j = a.units[u0 + e];
       if (j < 0 || j >= a.n_rows_units) {
         set_error(a.hdr, DV_ERR_INDEX_RANGE, j);
         j = -1;
       }
       unit_s[e] = j;
     }
-    __syncthreads();
-    const int r_lo = ub * a.rpu, r_hi = min(R, (ub + un) * a.rpu);
-    for (int r0 = r_lo + rg; r0 < r_hi; r0 += kPL * kNRG) {
-      uint4 wv[kPL];
-      int wrow[kPL];
+    // this thread's coefficients, in the same round trip as the unit ids
+    float cf[kPL][BT];
 #pragma unroll
-      for (int q = 0; q < kPL; ++q) {
-        const int r = r0 + q * kNRG;
-        wrow[q] = -1;
-        if (r < r_hi && chunk < C) {
-          const int u = r / a.rpu, t = r - u * a.rpu;
-          const int j = unit_s[u - ub];
-          if (j >= 0) {
-            wrow[q] = r;
-            wv[q] = ld_stream(W + ((size_t)j * a.rpu + t) * a.d + (size_t)chunk * V);
-          }
+    for (int q = 0; q < kPL; ++q) {
+      const int r = rb + rg + q * kNRG;
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+        cf[q][b] = (r < re && b < nb) ? a.coef[(size_t)(b0 + b) * a.coef_stride + r] : 0.f;
+    }
+    __syncthreads();
+    uint4 wv[kPL];
+    int jr[kPL];
+#pragma unroll
+    for (int q = 0; q < kPL; ++q) {
+      const int r = rb + rg + q * kNRG;
+      jr[q] = -1;
+      if (r < re && chunk < C) {
+        const int u = r / a.rpu;
+        const int j = unit_s[u - u0];
+        if (j >= 0) {
+          jr[q] = j;
+          wv[q] = ld_stream(W + ((size_t)j * a.rpu + (r - u * a.rpu)) * a.d + (size_t)chunk * V);
         }
       }
+    }
 #pragma unroll
-      for (int q = 0; q < kPL; ++q) {
-        if (wrow[q] < 0) continue;
-        const int r = wrow[q];
-        float wf[V];
-        unpack<T>(wv[q], wf);
+    for (int q = 0; q < kPL; ++q) {
+      if (jr[q] < 0) continue;
+      float wf[V];
+      unpack<T>(wv[q], wf);
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          if (b >= nb) break;
-          const int bb = b0 + b;
-          if (a.member) {
-            const int u = r / a.rpu;
-            if (!bit_test(a.member + (size_t)bb * a.words, unit_s[u - ub])) continue;
-          }
-          const float cf = a.coef[(size_t)bb * a.coef_stride + r];
+      for (int b = 0; b < BT; ++b) {
+        if (b >= nb) break;
+        if (a.member && !bit_test(a.member + (size_t)(b0 + b) * a.words, jr[q])) continue;
 #pragma unroll
-          for (int v = 0; v < V; ++v) acc[b][v] = fmaf(cf, wf[v], acc[b][v]);
-        }
+        for (int v = 0; v < V; ++v) acc[b][v] = fmaf(cf[q][b], wf[v], acc[b][v]);
       }
     }
   }
@@ -108,38 +112,41 @@ __global__ void __launch_bounds__(kThreads) rows_combine_kernel(CombineLaunch a,
     const int cc = e / (BT * V), b = (e / V) % BT, v = e % V;
     const int ch = blockIdx.x * kCW + cc;
     if (b >= nb || ch >= C) continue;
-    float s = 0.f;
+    float sm = 0.f;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s += red[w][cc][b][v];
+    for (int w = 0; w < kThreads / 32; ++w) sm += red[w][cc][b][v];
     float* o = a.out + (size_t)(b0 + b) * a.d + (size_t)ch * V + v;
-    *o = a.accumulate ? *o + s : s;
+    *o = a.accumulate ? *o + sm : sm;
   }
 }
 
-}  // namespace
-
-cudaError_t launch_rows_combine(const CombineLaunch& a, dv_dtype dt, cudaStream_t stream) {
-  const int V = dt == DV_F32 ? 4 : 8;
-  const int grid = (a.d / V + kCW - 1) / kCW;
+template <typename T>
+cudaError_t combine_t(const CombineLaunch& a, cudaStream_t stream) {
+  const int grid = (a.d / Elem<T>::kVec + kCW - 1) / kCW;
   for (int b0 = 0; b0 < a.B;) {
     const int nb = a.B - b0;
     const int bt = nb >= 4 ? 4 : (nb >= 2 ? 2 : 1);
-    switch (dt * 8 + bt) {
-      case DV_F32 * 8 + 4: rows_combine_kernel<float, 4><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_F32 * 8 + 2: rows_combine_kernel<float, 2><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_F32 * 8 + 1: rows_combine_kernel<float, 1><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_F16 * 8 + 4: rows_combine_kernel<__half, 4><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_F16 * 8 + 2: rows_combine_kernel<__half, 2><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_F16 * 8 + 1: rows_combine_kernel<__half, 1><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_BF16 * 8 + 4: rows_combine_kernel<__nv_bfloat16, 4><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case DV_BF16 * 8 + 2: rows_combine_kernel<__nv_bfloat16, 2><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      default: rows_combine_kernel<__nv_bfloat16, 1><<<grid, kThreads, 0, stream>>>(a, b0); break;
+    switch (bt) {
+      case 4: rows_combine_kernel<T, 4><<<grid, kThreads, 0, stream>>>(a, b0); break;
+      case 2: rows_combine_kernel<T, 2><<<grid, kThreads, 0, stream>>>(a, b0); break;
+      default: rows_combine_kernel<T, 1><<<grid, kThreads, 0, stream>>>(a, b0); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     b0 += bt;
   }
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_rows_combine(const CombineLaunch& a, dv_dtype dt, cudaStream_t stream) {
+  switch (dt) {
+    case DV_F32: return combine_t<float>(a, stream);
+    case DV_F16: return combine_t<__half>(a, stream);
+    case DV_BF16: return combine_t<__nv_bfloat16>(a, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dv

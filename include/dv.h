@@ -220,8 +220,10 @@ dv_status dv_sparse_attn_workspace_size(int B, int d, int h, int d_h, int cap,
  * S_b = head_idx[b][0 .. head_count[b]); pos [B] is device memory.
  * scale multiplies the logits (1/sqrt(d_h) for the usual convention; the
  * page's formula prints none).  out [B][d] fp32, see dv_sparse_mlp for
- * `accumulate`.  Limits: B <= 32, d_h in {64, 128}, h <= 256,
- * n_max <= 65536. */
+ * `accumulate`.  Limits: B <= 32, d_h in {64, 128}, h <= 1024,
+ * n_max <= 65536 (a multiple of 16), and one projection row of at most
+ * 40 KB (d <= 20480 for 16-bit types, 10240 for DV_F32); other head
+ * dimensions and rows return DV_ERR_UNSUPPORTED. */
 dv_status dv_sparse_attn(const void* y, int B, int d, int h, int d_h,
                          const void* Wqkv, const void* Wo, const dv_kv* kv,
                          const int32_t* pos, const int32_t* head_idx, int cap,
