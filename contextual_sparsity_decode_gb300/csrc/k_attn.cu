@@ -58,9 +58,6 @@ struct AttnArgs {
 __device__ __forceinline__ bool member_of(const AttnArgs& a, int b, int i) {
   return a.member ? bit_test(a.member + (size_t)b * a.hwords, i) : true;
 }
-__device__ __forceinline__ int union_count(const AttnArgs& a) {
-  return max(0, min(*a.U_count, a.capU));
-}
 __device__ __forceinline__ int row_pos(const AttnArgs& a, int b) {
   const int p = a.pos[b];
   return (p >= 0 && p < a.n_max) ? p : -1;
@@ -77,18 +74,18 @@ __device__ __forceinline__ int row_pos(const AttnArgs& a, int b) {
 // current token of every batch row that selected the head, and (K/V rows)
 // the stored embedding X[j] of every position j < pos whose K/V were skipped.
 
-constexpr int kQC = 4;      // chunks per thread per pass over a row
+constexpr int kQCMax = 4;   // chunks per thread per pass over a row (3 or 4)
 constexpr int kQR = 4;      // rows per thread group (divides d_h)
 constexpr int kNE = 2;      // vectors per group of entries
 constexpr int kWin = 4096;  // positions scanned per repair window (256 x 16)
 
 int qkv_tpr_log2(int chunks) {
   int l = 5;
-  while (l < 8 && (1 << l) * kQC < chunks) ++l;
+  while (l < 8 && (1 << l) * kQCMax < chunks) ++l;
   return l;
 }
 
-template <typename T>
+template <typename T, int kQC>
 __device__ __forceinline__ void qkv_load_w(const T* wbase, int d, int C, int cb, int tt, int tpr,
                                            uint4 (&w)[kQR][kQC]) {
   constexpr int V = Elem<T>::kVec;
@@ -102,11 +99,15 @@ __device__ __forceinline__ void qkv_load_w(const T* wbase, int d, int C, int cb,
 }
 
 // Dots the CTA's rows with entries ent[0..n) and stores the results (q in
-// fp32, K/V rounded to the storage type).  Called by all threads.
-template <typename T>
+// fp32, K/V rounded to the storage type).  Called by all threads.  After the
+// multiply-adds of the last group, `after_last_fma()` runs (all threads) while
+// the partial sums wait in registers: the persistent kernel uses it to issue
+// the next tile's weight loads into `w`.
+template <typename T, int kQC, typename F>
 __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)[kQR][kQC],
                             bool one_pass, const T* wbase, int tl, int m, int tbase, int i, int u,
-                            float (&red)[8][kQR][kNE], const uint4 (&ycur)[kQC], bool ycur_ok) {
+                            float (&red)[8][kQR][kNE], const uint4 (&ycur)[kQC], bool ycur_ok,
+                            F&& after_last_fma) {
   constexpr int V = Elem<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int tpr = 1 << tl, RS = 256 >> tl, tt = tid & (tpr - 1);
@@ -121,7 +122,7 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
 #pragma unroll
       for (int e = 0; e < kNE; ++e) acc[k][e] = 0.f;
     for (int cb = 0; cb < C; cb += tpr * kQC) {
-      if (!one_pass) qkv_load_w<T>(wbase, a.d, C, cb, tt, tpr, w);
+      if (!one_pass) qkv_load_w<T, kQC>(wbase, a.d, C, cb, tt, tpr, w);
 #pragma unroll
       for (int j = 0; j < kQC; ++j) {
         const int c = cb + tt + j * tpr;
@@ -145,6 +146,7 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
         }
       }
     }
+    if (g0 + kNE >= n) after_last_fma();
 #pragma unroll
     for (int k = 0; k < kQR; ++k)
 #pragma unroll
@@ -171,26 +173,30 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
     }
     __syncthreads();  // red is rewritten by the next group
   }
+  if (n == 0) after_last_fma();
 }
 
-template <typename T>
+// Persistent over tiles: CTA b takes tiles b, b + G, ... (a tile = rpc rows of
+// one selected head's W^Q, W^K or W^V block).  The next tile's weights (and,
+// batch 1, its valid flags) are requested right after the current tile's
+// multiply-adds, so they are in flight during its reduction and stores.
+template <typename T, int kQC>
 __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, int tl) {
   constexpr int V = Elem<T>::kVec;
   __shared__ int ent[kWin];
   __shared__ int n_ent;
   __shared__ float red[8][kQR][kNE];
+  __shared__ int U_s[1024];
   const int tid = threadIdx.x;
   const int tpr = 1 << tl, RS = 256 >> tl, slot = tid >> tl, tt = tid & (tpr - 1);
   const int rpc = RS * kQR;
-  const int u = blockIdx.x / RG, rg = blockIdx.x % RG;
-  const int r0 = rg * rpc;        // first row of the CTA within the head's 3 d_h rows
-  const int m = r0 / a.d_h;       // 0 = Q, 1 = K, 2 = V
-  const int tbase = r0 - m * a.d_h;
+  const int G = (int)gridDim.x;
   const int C = a.d / V;
   const bool one_pass = C <= tpr * kQC;
-  // round trip 1: head index (u < capU keeps it in bounds), count, position
-  // and (batch 1) this thread's chunks of the current token
-  const int i = a.U[u];
+  // round trip 1: count, head list, position and (batch 1) this thread's
+  // chunks of the current token
+  const int cnt_raw = *a.U_count;
+  for (int e = tid; e < a.capU; e += 256) U_s[e] = a.U[e];
   const int p0 = a.B == 1 ? row_pos(a, 0) : -1;
   const bool ycur_ok = a.B == 1 && one_pass;
   uint4 ycur[kQC];
@@ -201,56 +207,97 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
       if (c < C) ycur[j] = ld_cached(static_cast<const T*>(a.y) + (size_t)c * V);
     }
   }
-  if (u >= union_count(a)) return;
-  if (i < 0 || i >= a.h) {
-    if (tid == 0 && rg == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
-    return;
-  }
-  // round trip 2: the weights and (batch 1, K/V rows) the valid flags
-  const T* wbase = static_cast<const T*>(a.Wqkv) +
-                   ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
-  uint4 w[kQR][kQC];
-  if (one_pass) qkv_load_w<T>(wbase, a.d, C, 0, tt, tpr, w);
-  const bool fast_scan = a.B == 1 && m > 0 && p0 >= 0 && p0 <= kWin;
-  uint4 vflags = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
-  if (fast_scan && tid * 16 < p0)
-    vflags = *reinterpret_cast<const uint4*>(a.valid + (size_t)i * a.n_max + tid * 16);
+  const int nU = max(0, min(cnt_raw, a.capU));
+  const int ntiles = nU * RG;
+  if ((int)blockIdx.x >= ntiles) return;  // uniform, before any barrier
+  __syncthreads();
 
-  if (tid == 0) n_ent = 0;
-  __syncthreads();
-  for (int b = tid; b < a.B; b += blockDim.x) {
-    const int p = row_pos(a, b);
-    if (p >= 0 && member_of(a, b, i)) ent[atomicAdd(&n_ent, 1)] = kCur | (b << 20) | p;
-  }
-  __syncthreads();
-  qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok);
-  if (m == 0) return;
-  // K/V rows: positions whose K/V were skipped, one window of 4096 at a time
-  for (int b = 0; b < a.B; ++b) {
-    const int p = row_pos(a, b);
-    if (p < 0 || !member_of(a, b, i)) continue;
-    const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
-    for (int base = 0; base < p; base += kWin) {
-      const int j0 = base + tid * 16;
-      const uint4 v4 = fast_scan ? vflags
-                       : (j0 < p ? *reinterpret_cast<const uint4*>(vr + j0)
-                                 : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu));
-      const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
-      int mine = 0;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        mine += (j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0);
-      if (!__syncthreads_or(mine)) continue;  // nothing to repair in this window
-      if (tid == 0) n_ent = 0;
-      __syncthreads();
+  uint4 w[kQR][kQC];
+  uint4 vflags = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+  auto meta = [&](int t, int& i, int& m, int& tbase, int& u) {
+    u = t / RG;
+    const int r0 = (t - u * RG) * rpc;
+    i = U_s[u];
+    m = r0 / a.d_h;
+    tbase = r0 - m * a.d_h;
+  };
+  auto fetch = [&](int t) {  // weights (one pass) and batch-1 valid flags of tile t
+    int i, m, tbase, u;
+    meta(t, i, m, tbase, u);
+    if (i < 0 || i >= a.h) return;
+    const T* wb = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
+    if (one_pass) qkv_load_w<T, kQC>(wb, a.d, C, 0, tt, tpr, w);
+    vflags = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+    if (a.B == 1 && m > 0 && p0 >= 0 && p0 <= kWin && tid * 16 < p0)
+      vflags = *reinterpret_cast<const uint4*>(a.valid + (size_t)i * a.n_max + tid * 16);
+  };
+  fetch(blockIdx.x);
+
+  for (int t = blockIdx.x; t < ntiles; t += G) {
+    int i, m, tbase, u;
+    meta(t, i, m, tbase, u);
+    const int tn = t + G;
+    if (i < 0 || i >= a.h) {
+      if (tid == 0 && tbase == 0 && m == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
+      if (tn < ntiles) fetch(tn);
+      continue;
+    }
+    const T* wbase = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
+    const bool fast_scan = a.B == 1 && m > 0 && p0 >= 0 && p0 <= kWin;
+    const uint4 vf = vflags;
+    // entries: the current token of every row that selected head i, then
+    // (K/V rows) the positions whose K/V were skipped; the batch-1 fast path
+    // uses the prefetched flags (one window)
+    if (tid == 0) n_ent = 0;
+    __syncthreads();
+    for (int b = tid; b < a.B; b += blockDim.x) {
+      const int p = row_pos(a, b);
+      if (p >= 0 && member_of(a, b, i)) ent[atomicAdd(&n_ent, 1)] = kCur | (b << 20) | p;
+    }
+    if (fast_scan) {
+      const int j0 = tid * 16;
+      const uint32_t w4[4] = {vf.x, vf.y, vf.z, vf.w};
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int j = j0 + k;
-        if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0) ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
+        if (j < p0 && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0) ent[atomicAdd(&n_ent, 1)] = j;
       }
-      __syncthreads();
-      qkv_entries<T>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false);
     }
+    __syncthreads();
+    const int n_first = n_ent;
+    qkv_entries<T, kQC>(a, ent, n_first, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok, [&]() {
+      if (!(m > 0 && !fast_scan) && tn < ntiles) fetch(tn);
+    });
+    if (m > 0 && !fast_scan) {
+      // general path (batch > 1 or pos > 4096): windows of 4096 positions
+      for (int b = 0; b < a.B; ++b) {
+        const int p = row_pos(a, b);
+        if (p < 0 || !member_of(a, b, i)) continue;
+        const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
+        for (int base = 0; base < p; base += kWin) {
+          const int j0 = base + tid * 16;
+          const uint4 v4 = j0 < p ? *reinterpret_cast<const uint4*>(vr + j0)
+                                  : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+          const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+          int mine = 0;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            mine += (j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0);
+          if (!__syncthreads_or(mine)) continue;
+          if (tid == 0) n_ent = 0;
+          __syncthreads();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int j = j0 + k;
+            if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0) ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
+          }
+          __syncthreads();
+          qkv_entries<T, kQC>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false, []() {});
+        }
+      }
+      if (tn < ntiles) fetch(tn);
+    }
+    __syncthreads();  // ent / n_ent are rebuilt for the next tile
   }
 }
 
@@ -677,7 +724,14 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   // 1. projections + fused repair
   const int tl = qkv_tpr_log2(a.d / Elem<T>::kVec);
   const int RG = 3 * a.d_h / ((256 >> tl) * kQR);
-  attn_qkv_kernel<T><<<a.capU * RG, 256, 0, stream>>>(a, RG, tl);
+  if (a.capU > 1024) return cudaErrorInvalidValue;
+  const int tiles = a.capU * RG;
+  const int grid = tiles < 2 * num_sms ? tiles : 2 * num_sms;  // two resident CTAs per SM
+  // three chunks per thread when a row fits (fewer registers), else four
+  if (a.d / Elem<T>::kVec <= (1 << tl) * 3)
+    attn_qkv_kernel<T, 3><<<grid, 256, 0, stream>>>(a, RG, tl);
+  else
+    attn_qkv_kernel<T, 4><<<grid, 256, 0, stream>>>(a, RG, tl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 2. split-KV softmax, one cluster per (row, head), cache bookkeeping
