@@ -127,6 +127,15 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* tmp, int* total)
   return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream still runs;
+// grid_dep_wait() blocks until the predecessor has completed and its writes
+// are visible, so only data the predecessor does not write may be read
+// before it.  grid_dep_launch() lets the successor start early.  Both are
+// no-ops for kernels launched the ordinary way.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // L2 prefetch of a contiguous byte range (address 16-byte aligned, size a
 // multiple of 16): starts the HBM read without staging it anywhere.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {

@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   const int G = (int)gridDim.x;
   const int C = a.d / V;
   const bool one_pass = C <= tpr * kQC;
+  grid_dep_launch();  // the decode kernel may start reading its head lists
   // round trip 1: count, head list, position and (batch 1) this thread's
   // chunks of the current token
   const int cnt_raw = *a.U_count;
@@ -367,6 +368,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   const int p = row_pos(a, b);
   if (s == a.cap) {  // housekeeping of row b (rank 0 only): append X[p], reset the valid column
     if (rank != 0) return;
+    grid_dep_wait();
     if (p < 0) {
       if (tid == 0) set_error(a.hdr, DV_ERR_POSITION, a.pos[b]);
       return;
@@ -401,6 +403,9 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   const int i = a.head_idx[(size_t)b * a.cap + s];
   const int cnt = max(0, min(cnt_raw, a.cap));
   if (s >= cnt) return;  // the whole cluster agrees
+  // q, K and V come from attn_qkv: everything below waits for it
+  grid_dep_wait();
+  grid_dep_launch();
   if (i < 0 || i >= a.h) {
     if (tid == 0 && rank == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
     return;
@@ -699,18 +704,7 @@ int decode_cluster_width() {
 template <typename T, int DH>
 cudaError_t launch_decode_dh(const AttnArgs& a, cudaStream_t stream) {
   const int cw = decode_cluster_width<T, DH>();
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cw, a.cap + 1, a.B);
-  cfg.blockDim = dim3(kDecThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = cw;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<T, DH>, a);
+  return launch_k(attn_decode_kernel<T, DH>, dim3(cw, a.cap + 1, a.B), dim3(kDecThreads), 0, stream, true, cw, a);
 }
 
 template <typename T>

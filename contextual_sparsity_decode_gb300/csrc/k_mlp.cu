@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
   const int slot = tid >> a.tl, tt = tid & (tpr - 1);
   const int row0 = (blockIdx.x * RS + slot) * kR;  // positions in the list
   const int C = a.d / V;
+  grid_dep_launch();  // the down-projection may start loading its rows
   const int nb = min(BT, a.B - a.b0);
   // list entries are read in parallel with the count (positions < cap are in bounds)
   int nid[kR];

@@ -37,6 +37,7 @@ struct RowArgs {
   RowSeg seg[2];
   int nseg;
   int B, b0;
+  int pdl;  // launched programmatically: x is the predecessor's output
 };
 
 // Threads per row: the smallest power of two in [32, 256] covering the row's
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) rows_dot(RowArgs a) {
   for (int k = 0; k < kR; ++k)
 #pragma unroll
     for (int b = 0; b < BT; ++b) acc[k][b] = 0.f;
+  if (!a.pdl) grid_dep_launch();
 
   for (int cb = 0; cb < C; cb += tpr * kC) {
     uint4 w[kR][kC];
@@ -84,6 +86,10 @@ __global__ void __launch_bounds__(kThreads) rows_dot(RowArgs a) {
         const int c = cb + tt + j * tpr;
         if (row0 + k < rows && c < C) w[k][j] = ld_stream(W + (size_t)(row0 + k) * K + (size_t)c * V);
       }
+    if (a.pdl && cb == 0) {  // the weights are in flight; x comes from the predecessor
+      grid_dep_wait();
+      grid_dep_launch();
+    }
 #pragma unroll
     for (int j = 0; j < kC; ++j) {
       const int c = cb + tt + j * tpr;
@@ -175,6 +181,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
   int32_t* count = p1 ? a.count[1] : a.count[0];
   const float* s = (p1 ? a.s[1] : a.s[0]) + (size_t)b * N;
   int32_t* out = (p1 ? a.idx[1] : a.idx[0]) + (size_t)b * cap;
+  grid_dep_wait();  // the scores are the predecessor's output
 
   // stage the scores: kSelLoads independent loads per thread per round trip
   uint32_t lo = 0xffffffffu, hi = 0u;
@@ -296,8 +303,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
 
 template <typename T, typename XT, int EPI, int BT>
 cudaError_t launch_rows(RowArgs a, int grid, cudaStream_t stream) {
-  rows_dot<T, XT, EPI, BT><<<grid, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_k(rows_dot<T, XT, EPI, BT>, dim3(grid), dim3(kThreads), 0, stream, a.pdl != 0, 1, a);
 }
 
 // One launch per batch tile of up to 8 rows; the two segments' CTAs are laid
@@ -342,6 +348,7 @@ cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_pr
   RowArgs g2{};
   g2.nseg = n_preds;
   g2.B = B;
+  g2.pdl = 1;
   for (int i = 0; i < n_preds; ++i) g2.seg[i] = RowSeg{p.P2t[i], p.h[i], p.s[i], p.N[i], p.r[i], 0, 0};
   e = run_rows<T, float, kSigmoid>(g2, stream);
   if (e != cudaSuccess) return e;
@@ -361,8 +368,7 @@ cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_pr
     if (ea != cudaSuccess) return ea;
     attr_set = true;
   }
-  select_kernel<<<dim3(B, n_preds), kSelThreads, smem, stream>>>(sa, hdr);
-  return cudaGetLastError();
+  return launch_k(select_kernel, dim3(B, n_preds), dim3(kSelThreads), smem, stream, true, 1, sa, hdr);
 }
 
 }  // namespace

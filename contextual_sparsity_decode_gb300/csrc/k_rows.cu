@@ -57,15 +57,6 @@ __global__ void __launch_bounds__(kThreads) rows_combine_kernel(CombineLaunch a,
       }
       unit_s[e] = j;
     }
-    // this thread's coefficients, in the same round trip as the unit ids
-    float cf[kPL][BT];
-#pragma unroll
-    for (int q = 0; q < kPL; ++q) {
-      const int r = rb + rg + q * kNRG;
-#pragma unroll
-      for (int b = 0; b < BT; ++b)
-        cf[q][b] = (r < re && b < nb) ? a.coef[(size_t)(b0 + b) * a.coef_stride + r] : 0.f;
-    }
     __syncthreads();
     uint4 wv[kPL];
     int jr[kPL];
@@ -81,6 +72,18 @@ __global__ void __launch_bounds__(kThreads) rows_combine_kernel(CombineLaunch a,
           wv[q] = ld_stream(W + ((size_t)j * a.rpu + (r - u * a.rpu)) * a.d + (size_t)chunk * V);
         }
       }
+    }
+    // The unit ids and rows above do not depend on the predecessor kernel
+    // (it produces only the coefficients), so they were requested before
+    // waiting for it.
+    if (rb == 0) grid_dep_wait();
+    float cf[kPL][BT];
+#pragma unroll
+    for (int q = 0; q < kPL; ++q) {
+      const int r = rb + rg + q * kNRG;
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+        cf[q][b] = (r < re && b < nb) ? a.coef[(size_t)(b0 + b) * a.coef_stride + r] : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < kPL; ++q) {
@@ -126,12 +129,12 @@ cudaError_t combine_t(const CombineLaunch& a, cudaStream_t stream) {
   for (int b0 = 0; b0 < a.B;) {
     const int nb = a.B - b0;
     const int bt = nb >= 4 ? 4 : (nb >= 2 ? 2 : 1);
+    cudaError_t e;
     switch (bt) {
-      case 4: rows_combine_kernel<T, 4><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      case 2: rows_combine_kernel<T, 2><<<grid, kThreads, 0, stream>>>(a, b0); break;
-      default: rows_combine_kernel<T, 1><<<grid, kThreads, 0, stream>>>(a, b0); break;
+      case 4: e = launch_k(rows_combine_kernel<T, 4>, dim3(grid), dim3(kThreads), 0, stream, true, 1, a, b0); break;
+      case 2: e = launch_k(rows_combine_kernel<T, 2>, dim3(grid), dim3(kThreads), 0, stream, true, 1, a, b0); break;
+      default: e = launch_k(rows_combine_kernel<T, 1>, dim3(grid), dim3(kThreads), 0, stream, true, 1, a, b0); break;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     b0 += bt;
   }
