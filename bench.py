@@ -140,6 +140,37 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def _csrc_sha256():
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "contextual_sparsity_decode_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                   glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic():
+    """DRAM bytes per entry-point call from the committed ncu capture, or {}
+    when the kernel sources changed since it was taken."""
+    try:
+        vals = {}
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.txt")) as f:
+            for line in f:
+                if "=" in line and not line.lstrip().startswith("#"):
+                    k, v = (x.strip() for x in line.split("=", 1))
+                    vals[k] = v
+        if vals.get("csrc_sha256") != _csrc_sha256():
+            return {}
+        return {k: float(v) for k, v in vals.items() if k != "csrc_sha256"}
+    except (OSError, ValueError):
+        return {}
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -256,12 +287,13 @@ def run_ours(args, rank, world, local):
     dec.capture(advance=(w.n_prompt, w.n_max))
     peak, peak_kind = _peaks()
     dom = max(fam, key=lambda k: fam[k]["us_per_launch"] * fam[k]["launches_per_step"])
-    kernel_names = {"mlp": "sparse_mlp_kernel (dv_sparse_mlp)",
-                    "attn": "attn_qkv + attn_decode + attn_out (dv_sparse_attn)",
-                    "predict": "predict_gemv x2 + select (dv_predict / dv_lookahead)"}
+    kernel_names = {"mlp": "dv_sparse_mlp: mlp_up_kernel + rows_combine_kernel",
+                    "attn": "dv_sparse_attn: attn_qkv_kernel + attn_decode_kernel + rows_combine_kernel",
+                    "predict": "dv_predict: rows_dot x2 + select_kernel"}
+    traffic = _traffic().get({"mlp": "dv_sparse_mlp", "attn": "dv_sparse_attn", "predict": "dv_predict"}[dom])
     roof = {"bound": "hbm", "kernel": kernel_names[dom], "achieved": fam[dom]["gbs"],
             "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
-            "frac": (fam[dom]["gbs"] / peak) if fam[dom]["gbs"] else None, "traffic": None,
+            "frac": (fam[dom]["gbs"] / peak) if fam[dom]["gbs"] else None, "traffic": traffic,
             "bytes_per_launch": fam[dom]["bytes_per_launch"]}
 
     # ---- end to end through the public API with host buffers
@@ -282,7 +314,10 @@ def run_ours(args, rank, world, local):
     e2e = {"value": tokens / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": 4 * w.d,
            "d2h_bytes_per_step": 4 * w.d}
 
-    launches_per_step = w.layers * 6 + (w.layers - 1) * 3 + 3 + 1
+    # per layer: 2 layernorms, 3 attention kernels, 2 MLP kernels, 3 predictor
+    # kernels (layer 0 on the main stream, the look-ahead ones on the side
+    # stream); one position update per token
+    launches_per_step = w.layers * (2 + 3 + 2 + 3) + 1
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
