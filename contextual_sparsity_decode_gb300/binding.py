@@ -36,7 +36,7 @@ EXPORTS = (
     "dv_predict_workspace_size", "dv_predict", "dv_lookahead", "dv_predict_static",
     "dv_sparse_mlp_workspace_size", "dv_sparse_mlp",
     "dv_sparse_attn_workspace_size", "dv_sparse_attn", "dv_kv_repair",
-    "dv_layernorm", "dv_positions_advance",
+    "dv_layernorm", "dv_positions_advance", "dv_set_launch_overlap",
 )
 
 
@@ -86,6 +86,7 @@ _SIGS = {
                       _vp, _c_int, _vp, _sz, _vp], _c_int),
     "dv_layernorm": ([_vp, _c_int, _c_int, _c_float, _vp, _c_int, _vp], _c_int),
     "dv_positions_advance": ([_vp, _c_int, _c_int, _c_int, _vp], _c_int),
+    "dv_set_launch_overlap": ([_c_int], _c_int),
 }
 
 
@@ -309,3 +310,9 @@ def dv_layernorm(x: torch.Tensor, y: torch.Tensor, eps: float = 1e-5, stream=Non
 def dv_positions_advance(pos: torch.Tensor, lo: int, hi: int, stream=None):
     _ok(lib().dv_positions_advance(_ptr(pos), pos.numel(), int(lo), int(hi), _stream(stream)),
         "dv_positions_advance")
+
+
+def dv_set_launch_overlap(level: int) -> int:
+    """Process-wide launch policy (see dv_set_launch_overlap in dv.h);
+    returns the previous level."""
+    return int(lib().dv_set_launch_overlap(int(level)))

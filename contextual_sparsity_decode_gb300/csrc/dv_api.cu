@@ -195,6 +195,8 @@ int dv_last_cuda_error(void) { return g_last_cuda_error; }
 
 int dv_version(void) { return 100; }
 
+int dv_set_launch_overlap(int level) { return set_launch_overlap(level); }
+
 dv_status dv_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!ws || ws_bytes < sizeof(WsHeader)) return DV_ERR_INVALID_ARG;
   cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, stream);

@@ -43,6 +43,11 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Launch policy (dv_set_launch_overlap): 1 lets the first kernel of a batch-1
+// attention or MLP call start during the kernel before the call (k_misc.cu).
+int launch_overlap();
+int set_launch_overlap(int level);
+
 // ---- predictor (k_predict.cu) ----------------------------------------------
 
 // Largest unit count a selection CTA stages in shared memory (208 KB).

@@ -181,7 +181,7 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
 // batch 1, its valid flags) are requested right after the current tile's
 // multiply-adds, so they are in flight during its reduction and stores.
 template <typename T, int kQC>
-__global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, int tl) {
+__global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, int tl, int pdl) {
   constexpr int V = Elem<T>::kVec;
   __shared__ int ent[kWin];
   __shared__ int n_ent;
@@ -193,7 +193,10 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   const int G = (int)gridDim.x;
   const int C = a.d / V;
   const bool one_pass = C <= tpr * kQC;
-  grid_dep_launch();  // the decode kernel may start reading its head lists
+  // Launched with overlap (pdl), the kernel may start while the producer of
+  // y still runs: head list, count, position, valid flags and weights are
+  // read before grid_dep_wait(), y only after it.
+  if (!pdl) grid_dep_launch();  // the decode kernel may start reading its head lists
   // round trip 1: count, head list, position and (batch 1) this thread's
   // chunks of the current token
   const int cnt_raw = *a.U_count;
@@ -201,13 +204,16 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   const int p0 = a.B == 1 ? row_pos(a, 0) : -1;
   const bool ycur_ok = a.B == 1 && one_pass;
   uint4 ycur[kQC];
-  if (ycur_ok) {
+  auto load_ycur = [&]() {
+    if (ycur_ok) {
 #pragma unroll
-    for (int j = 0; j < kQC; ++j) {
-      const int c = tt + j * tpr;
-      if (c < C) ycur[j] = ld_cached(static_cast<const T*>(a.y) + (size_t)c * V);
+      for (int j = 0; j < kQC; ++j) {
+        const int c = tt + j * tpr;
+        if (c < C) ycur[j] = ld_cached(static_cast<const T*>(a.y) + (size_t)c * V);
+      }
     }
-  }
+  };
+  if (!pdl) load_ycur();
   const int nU = max(0, min(cnt_raw, a.capU));
   const int ntiles = nU * RG;
   if ((int)blockIdx.x >= ntiles) return;  // uniform, before any barrier
@@ -233,6 +239,11 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
       vflags = *reinterpret_cast<const uint4*>(a.valid + (size_t)i * a.n_max + tid * 16);
   };
   fetch(blockIdx.x);
+  if (pdl) {
+    grid_dep_wait();
+    grid_dep_launch();
+    load_ycur();
+  }
 
   for (int t = blockIdx.x; t < ntiles; t += G) {
     int i, m, tbase, u;
@@ -722,11 +733,12 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   const int tiles = a.capU * RG;
   const int grid = tiles < 2 * num_sms ? tiles : 2 * num_sms;  // two resident CTAs per SM
   // three chunks per thread when a row fits (fewer registers), else four
+  const int pdl = (launch_overlap() > 0 && a.B == 1) ? 1 : 0;
+  cudaError_t e;
   if (a.d / Elem<T>::kVec <= (1 << tl) * 3)
-    attn_qkv_kernel<T, 3><<<grid, 256, 0, stream>>>(a, RG, tl);
+    e = launch_k(attn_qkv_kernel<T, 3>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
   else
-    attn_qkv_kernel<T, 4><<<grid, 256, 0, stream>>>(a, RG, tl);
-  cudaError_t e = cudaGetLastError();
+    e = launch_k(attn_qkv_kernel<T, 4>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
   if (e != cudaSuccess) return e;
   // 2. split-KV softmax, one cluster per (row, head), cache bookkeeping
   e = launch_decode<T>(a, stream);

@@ -1,6 +1,8 @@
 // Decoder-step helpers: the pre-LayerNorm of each sparse block and the
 // position counter of a decode loop.
 
+#include <atomic>
+
 #include "dv_kernels.h"
 
 namespace dv {
@@ -51,6 +53,7 @@ template <typename T>
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float* x, int d, float eps, T* y) {
   __shared__ float red[kLnThreads / 32];
   const int b = blockIdx.x, tid = threadIdx.x;
+  grid_dep_launch();  // a consumer launched with overlap may start its own loads
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)b * d);
   const int n4 = d / 4;
   float4 v[kLnVec];
@@ -91,6 +94,13 @@ __global__ void positions_kernel(int32_t* pos, int B, int lo, int hi) {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_launch_overlap{0};
+}
+
+int launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed); }
+int set_launch_overlap(int level) { return g_launch_overlap.exchange(level > 0 ? 1 : 0); }
 
 cudaError_t launch_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtype dt,
                              cudaStream_t stream) {

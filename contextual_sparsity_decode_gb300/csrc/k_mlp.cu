@@ -35,6 +35,7 @@ struct UpArgs {
   int tl;                     // threads per row (log2)
   float* act;                 // [B][cap]
   WsHeader* hdr;
+  int pdl;                    // launched with overlap: y is read after grid_dep_wait()
 };
 
 int up_tpr_log2(int chunks) {
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
   const int slot = tid >> a.tl, tt = tid & (tpr - 1);
   const int row0 = (blockIdx.x * RS + slot) * kR;  // positions in the list
   const int C = a.d / V;
-  grid_dep_launch();  // the down-projection may start loading its rows
+  if (!a.pdl) grid_dep_launch();  // the down-projection may start loading its rows
   const int nb = min(BT, a.B - a.b0);
   // list entries are read in parallel with the count (positions < cap are in bounds)
   int nid[kR];
@@ -89,6 +90,10 @@ __global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
         const int c = cb + tt + j * tpr;
         if (nid[k] >= 0 && c < C) w[k][j] = ld_stream(W + (size_t)nid[k] * a.d + (size_t)c * V);
       }
+    if (a.pdl && cb == 0) {  // rows in flight; y comes from the kernel before the call
+      grid_dep_wait();
+      grid_dep_launch();
+    }
 #pragma unroll
     for (int j = 0; j < kC; ++j) {
       const int c = cb + tt + j * tpr;
@@ -183,8 +188,7 @@ __global__ void __launch_bounds__(1024) union_kernel(const int32_t* idx, int cap
 
 template <typename T, int BT>
 cudaError_t launch_up(const UpArgs& a, int grid, cudaStream_t stream) {
-  mlp_up_kernel<T, BT><<<grid, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_k(mlp_up_kernel<T, BT>, dim3(grid), dim3(kThreads), 0, stream, a.pdl != 0, 1, a);
 }
 
 template <typename T>
@@ -200,6 +204,7 @@ cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t s
     u.list = L.U; u.list_count = L.U_count; u.member = L.member; u.cap = mlp_union_cap(L.B, L.N, L.cap);
   }
   u.tl = up_tpr_log2(L.d / Elem<T>::kVec);
+  u.pdl = (launch_overlap() > 0 && L.B == 1) ? 1 : 0;
   const int rpc = (kThreads >> u.tl) * kR;
   const int grid = (u.cap + rpc - 1) / rpc;
   for (int b0 = 0; b0 < L.B;) {

@@ -112,6 +112,16 @@ class SparseDecoder:
 
     def step_ops(self):
         """Enqueue one token on the current stream (+ the side stream)."""
+        # Every attention / MLP call here directly follows the layernorm that
+        # produces its input, except layer 0's attention (after its predictor
+        # on the same stream): launch overlap is on for all the others.
+        prev = dv.dv_set_launch_overlap(1)
+        try:
+            self._step_ops()
+        finally:
+            dv.dv_set_launch_overlap(prev)
+
+    def _step_ops(self):
         main = torch.cuda.current_stream()
         for l in range(self.L):
             W = self.layers[l]
@@ -137,9 +147,12 @@ class SparseDecoder:
                     dv.dv_lookahead(self.y_a[l], self.predictors(l + 1), self.ws_pred_side,
                                     self.ev_y[l], self.side, self.ev_pred[l + 1])
             self._time("attn")
+            if l == 0:
+                dv.dv_set_launch_overlap(0)  # the predictor just wrote this call's head list
             dv.dv_sparse_attn(self.y_a[l], W["Wqkv"], W["Wo"], self.kv[l], self.pos,
                               self.head_idx[l], self.head_cnt[l], self.scale, self.r_stream,
                               self.ws_attn, accumulate=True)
+            dv.dv_set_launch_overlap(1)
             self._time("attn")
             dv.dv_layernorm(self.r_stream, self.y_m, self.eps)
             self._time("mlp")

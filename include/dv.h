@@ -252,6 +252,19 @@ dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h,
 dv_status dv_layernorm(const float* x, int B, int d, float eps,
                        void* y, dv_dtype dt, cudaStream_t stream);
 
+/* Launch policy (no counterpart in the pages; it changes timing, never
+ * results).  Inside every entry point the later kernels start during the
+ * earlier ones and read only data those do not write.  At level 0 (the
+ * default) the first kernel of each call waits for everything before it.
+ * At level 1, for batch 1, the first kernel of dv_sparse_attn and of
+ * dv_sparse_mlp may also start while the kernel before the call is still
+ * running, and reads before waiting for it: the head / neuron lists and
+ * counts, pos, the valid flags and the weights.  Enable it only when the
+ * kernel issued just before each such call (on the same stream) writes none
+ * of those -- true when that kernel is the dv_layernorm producing the call's
+ * y, as in a pre-LN decoder.  Process-wide; returns the previous level. */
+int dv_set_launch_overlap(int level);
+
 /* pos[b] = pos[b] + 1, or `lo` when that reaches `hi` (decode loop). */
 dv_status dv_positions_advance(int32_t* pos, int B, int lo, int hi,
                                cudaStream_t stream);

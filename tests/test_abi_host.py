@@ -121,3 +121,15 @@ def test_attention_arguments_rejected_on_host():
     assert st == 1
     assert lib.dv_layernorm(None, 1, 64, 1e-5, _vp(fake), dv.DV_F16, _vp(0)) == 1
     assert lib.dv_positions_advance(_vp(fake), 1, 5, 5, _vp(0)) == 1
+
+
+def test_launch_overlap_policy_round_trips():
+    """The launch policy is a host-side setting: it returns the previous level
+    and clamps to {0, 1}."""
+    prev = dv.dv_set_launch_overlap(1)
+    try:
+        assert dv.dv_set_launch_overlap(5) == 1
+        assert dv.dv_set_launch_overlap(0) == 1
+        assert dv.dv_set_launch_overlap(-3) == 0
+    finally:
+        dv.dv_set_launch_overlap(prev)
