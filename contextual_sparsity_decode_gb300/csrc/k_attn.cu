@@ -414,10 +414,44 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   const int i = a.head_idx[(size_t)b * a.cap + s];
   const int cnt = max(0, min(cnt_raw, a.cap));
   if (s >= cnt) return;  // the whole cluster agrees
-  // q, K and V come from attn_qkv: everything below waits for it
+  const bool head_ok = i >= 0 && i < a.h;
+  const int n_pos = p + 1;
+  const int per = (n_pos + CSd - 1) / CSd;
+  const int j_lo = min(n_pos, rank * per), j_hi = min(n_pos, j_lo + per);
+  const T* Kr = static_cast<const T*>(a.K) + ((size_t)b * a.h + (head_ok ? i : 0)) * a.n_max * DH + lane * E;
+  const T* Vr = static_cast<const T*>(a.V) + ((size_t)b * a.h + (head_ok ? i : 0)) * a.n_max * DH + lane * E;
+
+  // Before waiting for attn_qkv: the K/V of positions it will not write.  It
+  // writes only position p and the positions whose valid flag is 0 (repairs),
+  // so the warp's first batch is loaded now for every position < p that is
+  // valid; the others are loaded after the wait.  (The valid flags of this
+  // CTA's positions are written only by this CTA, after the wait.)
+  Raw kraw[kPB], vraw[kPB];
+  uint32_t pre = 0;  // bit s2: position jw_first + s2 loaded before the wait
+  const int jw_first = j_lo + wid * kPW;
+  const int jw1_first = min(j_hi, jw_first + kPW);
+  if (head_ok && p >= 0) {
+    const uint8_t* vrow0 = a.valid + ((size_t)b * a.h + i) * a.n_max;
+    uint8_t fl[kPB];
+#pragma unroll
+    for (int s2 = 0; s2 < kPB; ++s2) {
+      const int j = jw_first + s2;
+      fl[s2] = (j < jw1_first && j < p) ? vrow0[j] : 0;
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < kPB; ++s2) {
+      if (fl[s2] == 1) {
+        const int j = jw_first + s2;
+        kraw[s2] = KvRaw<T, E>::load(Kr + (size_t)j * DH);
+        vraw[s2] = KvRaw<T, E>::load(Vr + (size_t)j * DH);
+        pre |= 1u << s2;
+      }
+    }
+  }
+  // q and the rest of K/V come from attn_qkv: everything below waits for it
   grid_dep_wait();
   grid_dep_launch();
-  if (i < 0 || i >= a.h) {
+  if (!head_ok) {
     if (tid == 0 && rank == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
     return;
   }
@@ -430,30 +464,24 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   }
   cluster_arrive();  // every CTA must be running before peers push into rank 0
 
-  const int n_pos = p + 1;
-  const int per = (n_pos + CSd - 1) / CSd;
-  const int j_lo = min(n_pos, rank * per), j_hi = min(n_pos, j_lo + per);
-
   float qr[E];
   const float* qg = a.q + ((size_t)b * a.capU + u) * DH + lane * E;
 #pragma unroll
   for (int e = 0; e < E; ++e) qr[e] = qg[e] * a.scale;
-  const T* Kr = static_cast<const T*>(a.K) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
-  const T* Vr = static_cast<const T*>(a.V) + ((size_t)b * a.h + i) * a.n_max * DH + lane * E;
 
   float mw = -INFINITY, lw = 0.f, acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
 #pragma unroll 1
-  for (int jw0 = j_lo + wid * kPW; jw0 < j_hi; jw0 += kDecWarps * kPW) {
+  for (int jw0 = jw_first; jw0 < j_hi; jw0 += kDecWarps * kPW) {
     const int jw1 = min(j_hi, jw0 + kPW);
 #pragma unroll 1
     for (int jb = jw0; jb < jw1; jb += kPB) {
-      Raw kraw[kPB], vraw[kPB];
+      const uint32_t have = jb == jw_first ? pre : 0u;
 #pragma unroll
       for (int s2 = 0; s2 < kPB; ++s2) {
         const int j = jb + s2;
-        if (j < jw1) {
+        if (j < jw1 && !((have >> s2) & 1u)) {
           kraw[s2] = KvRaw<T, E>::load(Kr + (size_t)j * DH);
           vraw[s2] = KvRaw<T, E>::load(Vr + (size_t)j * DH);
         }
