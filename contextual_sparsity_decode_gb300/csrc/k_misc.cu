@@ -53,6 +53,9 @@ template <typename T>
 __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float* x, int d, float eps, T* y) {
   __shared__ float red[kLnThreads / 32];
   const int b = blockIdx.x, tid = threadIdx.x;
+  // Launched programmatically: the input is read only after the previous
+  // kernel has completed, so this is safe after any kernel.
+  grid_dep_wait();
   grid_dep_launch();  // a consumer launched with overlap may start its own loads
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)b * d);
   const int n4 = d / 4;
@@ -105,13 +108,17 @@ int set_launch_overlap(int level) { return g_launch_overlap.exchange(level > 0 ?
 cudaError_t launch_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtype dt,
                              cudaStream_t stream) {
   switch (dt) {
-    case DV_F32: layernorm_kernel<float><<<B, kLnThreads, 0, stream>>>(x, d, eps, static_cast<float*>(y)); break;
-    case DV_F16: layernorm_kernel<__half><<<B, kLnThreads, 0, stream>>>(x, d, eps, static_cast<__half*>(y)); break;
+    case DV_F32:
+      return launch_k(layernorm_kernel<float>, dim3(B), dim3(kLnThreads), 0, stream, true, 1, x, d, eps,
+                      static_cast<float*>(y));
+    case DV_F16:
+      return launch_k(layernorm_kernel<__half>, dim3(B), dim3(kLnThreads), 0, stream, true, 1, x, d, eps,
+                      static_cast<__half*>(y));
     case DV_BF16:
-      layernorm_kernel<__nv_bfloat16><<<B, kLnThreads, 0, stream>>>(x, d, eps, static_cast<__nv_bfloat16*>(y));
-      break;
+      return launch_k(layernorm_kernel<__nv_bfloat16>, dim3(B), dim3(kLnThreads), 0, stream, true, 1, x, d,
+                      eps, static_cast<__nv_bfloat16*>(y));
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_positions_advance(int32_t* pos, int B, int lo, int hi, cudaStream_t stream) {

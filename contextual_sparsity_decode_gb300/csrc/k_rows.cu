@@ -76,7 +76,10 @@ __global__ void __launch_bounds__(kThreads) rows_combine_kernel(CombineLaunch a,
     // The unit ids and rows above do not depend on the predecessor kernel
     // (it produces only the coefficients), so they were requested before
     // waiting for it.
-    if (rb == 0) grid_dep_wait();
+    if (rb == 0) {
+      grid_dep_wait();
+      grid_dep_launch();  // a following layernorm may be scheduled; it waits for this kernel
+    }
     float cf[kPL][BT];
 #pragma unroll
     for (int q = 0; q < kPL; ++q) {
