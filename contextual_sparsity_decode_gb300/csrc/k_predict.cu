@@ -150,26 +150,35 @@ struct SelArgs {
 constexpr int kSelThreads = 1024;
 constexpr int kBins = 4096;  // histogram bins per refinement level (12 bits)
 constexpr int kSelLoads = 16;  // score loads in flight per thread
+constexpr int kCand = 256;     // keys ranked directly in the cut's bin, at most
 
 // One CTA per (predictor, batch row).  The row's scores are staged in shared
 // memory as their IEEE bits (sigmoid outputs are >= 0, so the bits order like
 // the values).
 //
-// Top-k finds the exact k-th largest key T by refining a key range: each level
-// bins the keys inside the current range into <= 4096 equal-width bins
-// (width a power of two), finds the bin holding the k-th largest, and narrows
-// the range to it.  The first level spans [min, max] of the row, so 32-bit
-// keys need at most three levels, and only keys inside the range touch the
-// histogram.  Output: every key > T plus the lowest-index keys equal to T,
-// ascending.  Thread t owns the contiguous element range [t*E, (t+1)*E) with
-// E odd (conflict-free bank access), so a block prefix sum of per-thread
-// counts gives every selected element its output slot.
+// Top-k orders the elements by (key descending, index ascending) and finds
+// the k-th one, the cut (T, T_idx): element i is selected iff key_i > T, or
+// key_i == T and i <= T_idx.  One level bins the keys of [min, max] into
+// <= 4096 equal-width bins (width a power of two) and finds the bin holding
+// the cut.  When at most kCand keys share that bin they are ranked against
+// each other directly; otherwise further levels narrow the range to one key
+// value (32-bit keys need at most three levels, and only keys inside the
+// range touch the histogram) and the cut is the right count of lowest-index
+// keys equal to it.  Output ascending: thread t owns the contiguous element
+// range [t*E, (t+1)*E) with E odd (conflict-free bank access; E <= 53 for
+// N <= 53248, so its selections fit a 64-bit mask), and a block prefix sum
+// of per-thread counts gives every selected element its output slot.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader* hdr) {
   extern __shared__ uint32_t keys[];
   __shared__ int hist[kBins];
   __shared__ int tmp[32];
   __shared__ uint32_t rlo[32], rhi[32];
-  __shared__ int sel_bin, sel_above;
+  __shared__ int sel_bin, sel_above, sel_count;
+  __shared__ uint32_t cand_k[kCand];
+  __shared__ int cand_i[kCand];
+  __shared__ int n_cand;
+  __shared__ uint32_t cut_k;
+  __shared__ int cut_i;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int b = blockIdx.x;
   const bool p1 = blockIdx.y != 0;
@@ -240,11 +249,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
 
-  // current range [base, top]; `need` keys are still to be taken from it
+  // Level over the keys inside [base, top]: bins them into <= 4096 bins of
+  // width 2^shift, finds the bin holding the need-th largest key and
+  // narrows [base, top] to it.  Returns that bin's key count.
   uint32_t base = lo, top = hi;
   int need = k;
-#pragma unroll 1
-  while (top > base) {
+  auto level = [&]() -> int {
     const uint32_t span = top - base;
     const int shift = max(0, 32 - __clz((int)span) - 12);
     const int nbins = (int)(span >> shift) + 1;
@@ -263,7 +273,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
       v4[q] = j >= 0 ? hist[j] : 0;
       v += v4[q];
     }
-    const int incl = block_inclusive_scan<kSelThreads>(v, tmp, &total);
+    int tot;
+    const int incl = block_inclusive_scan<kSelThreads>(v, tmp, &tot);
     if (incl >= need && incl - v < need) {
       int above = incl - v;
 #pragma unroll
@@ -271,6 +282,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
         if (above + v4[q] >= need) {
           sel_bin = nbins - 1 - (4 * tid + q);
           sel_above = above;
+          sel_count = v4[q];
           break;
         }
         above += v4[q];
@@ -282,21 +294,78 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelArgs a, WsHeader
     const uint64_t nt = nb + ((1ull << shift) - 1);
     base = (uint32_t)nb;
     top = (uint32_t)(nt < (uint64_t)top ? nt : (uint64_t)top);
+    const int c = sel_count;
     __syncthreads();  // sel_* and hist are rewritten by the next level
+    return c;
+  };
+
+  // The k-th largest (key, lowest index first) element is the cut (T, T_idx):
+  // element i is selected iff keys[i] > T, or keys[i] == T and i <= T_idx.
+  int c = level();
+  if (c <= kCand) {
+    // Few keys share the cut's bin: rank them directly.  Candidate c is
+    // ranked by the candidates with a larger key or an equal key and a
+    // lower index; the one of rank need-1 is the cut.
+    if (tid == 0) n_cand = 0;
+    __syncthreads();
+    for (int i = tid; i < N; i += kSelThreads) {
+      const uint32_t kv = keys[i];
+      if (kv >= base && kv <= top) {
+        const int slot = atomicAdd(&n_cand, 1);
+        cand_k[slot] = kv;
+        cand_i[slot] = i;
+      }
+    }
+    __syncthreads();
+    if (tid < c) {
+      const uint32_t kc = cand_k[tid];
+      const int ic = cand_i[tid];
+      int rank = 0;
+      for (int j = 0; j < c; ++j) {
+        const uint32_t kj = cand_k[j];
+        rank += kj > kc || (kj == kc && cand_i[j] < ic);
+      }
+      if (rank == need - 1) {
+        cut_k = kc;
+        cut_i = ic;
+      }
+    }
+  } else {
+    // many keys in the bin: refine until one key value remains, then take
+    // the need-th lowest index among the keys equal to it
+#pragma unroll 1
+    while (top > base) c = level();
+    int eq = 0;
+    for (int i = i0; i < i1; ++i) eq += keys[i] == base;
+    int tot;
+    const int eq_incl = block_inclusive_scan<kSelThreads>(eq, tmp, &tot);
+    if (eq_incl >= need && eq_incl - eq < need) {
+      int left = need - (eq_incl - eq);
+      for (int i = i0; i < i1; ++i)
+        if (keys[i] == base && --left == 0) {
+          cut_k = base;
+          cut_i = i;
+          break;
+        }
+    }
   }
-  const uint32_t T = base;
-  int gt = 0, eq = 0;
-  for (int i = i0; i < i1; ++i) { gt += keys[i] > T; eq += keys[i] == T; }
-  const int eq_incl = block_inclusive_scan<kSelThreads>(eq, tmp, &total);
-  const int take_eq = max(0, min(eq, need - (eq_incl - eq)));
-  const int mine = gt + take_eq;
-  const int tk_incl = block_inclusive_scan<kSelThreads>(mine, tmp, &total);
-  int o = tk_incl - mine;
-  int eq_seen = 0;
+  __syncthreads();
+  const uint32_t T = cut_k;
+  const int Ti = cut_i;
+  // this thread's selected elements (at most 64: E <= 64 for N <= 65536)
+  uint64_t mask = 0;
   for (int i = i0; i < i1; ++i) {
-    bool take = keys[i] > T;
-    if (keys[i] == T) { take = eq_seen < take_eq; ++eq_seen; }
-    if (take) out[o++] = i;
+    const uint32_t kv = keys[i];
+    if (kv > T || (kv == T && i <= Ti)) mask |= 1ull << (i - i0);
+  }
+  const int mine = __popcll(mask);
+  int total_sel;
+  const int sel_incl = block_inclusive_scan<kSelThreads>(mine, tmp, &total_sel);
+  int o = sel_incl - mine;
+  while (mask) {
+    const int bit = __ffsll((long long)mask) - 1;
+    out[o++] = i0 + bit;
+    mask &= mask - 1;
   }
   if (tid == 0) count[b] = k;
 }

@@ -37,6 +37,8 @@ CASES = [
     ("batch8_bf16",      8, 1024, 16, 128, "bf16", [100] * 8,     128,  3,    4,     "isq",  None),
     ("all_heads_f16",    1, 256,  8,  64,  "f16",  [17],          32,   3,    8,     "isq",  None),
     ("random_sizes_f16", 2, 256,  8,  64,  "f16",  [9, 4],        48,   8,    "rnd", "isq",  None),
+    ("random_sizes_b1",  1, 384,  12, 64,  "f16",  [21],          48,   12,   "rnd", "isq",  None),
+    ("opt13b_b1_bf16",   1, 5120, 40, 128, "bf16", [300],         320,  2,    12,    "isq",  0.02),
 ]
 
 
@@ -98,6 +100,8 @@ def test_sparse_attn_parity(case):
 
     g = torch.Generator().manual_seed(zlib.crc32(name.encode()))
     cap = h if k == "rnd" else max(1, k)
+    # one workspace for every step, as a decode loop uses it
+    ws_s = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, cap, n_max))
     for step in range(steps):
         p = [prompt[b] + step for b in range(B)]
         if max(p) >= n_max:
@@ -110,7 +114,6 @@ def test_sparse_attn_parity(case):
             idx[b, : len(S)] = S
             cnt[b] = len(S)
         out = torch.full((B, d), 77.0, device=dev)
-        ws_s = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, cap, n_max))
         dv.dv_sparse_attn(y.to(dev), Wqkv_d, Wo_d, kv, torch.tensor(p, dtype=torch.int32, device=dev),
                           idx.to(dev), cnt.to(dev), scale, out, ws_s)
         st, info = dv.dv_check(ws_s)
@@ -145,6 +148,51 @@ def test_accumulate_into_residual():
         c = oracle.KVCache.empty(h, n_max, d_h, d, "f16")
         ref = oracle.sparse_attn(f64(y)[b], f64(Wqkv), f64(Wo), c, 0, S, 0.125)
         assert_rel_l2(f64(out)[b] - f64(base)[b], ref, "f16", "accumulate")
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_no_selected_head(accumulate):
+    """An empty head set: MHA = 0, so out becomes 0 (or keeps the residual),
+    and the cache still records the token (X[pos], valid = 0)."""
+    B, d, h, d_h, n_max = 1, 512, 8, 64, 32
+    Wqkv, Wo = _layer("nohead", d, h, d_h, "f16", None)
+    dev = "cuda"
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
+    pos = torch.tensor([5], dtype=torch.int32, device=dev)
+    idx = torch.full((1, 4), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    base = draw((B, d), 1.0, 305, "nohead/base", "f32").to(dev)
+    out = base.clone()
+    y = draw((B, d), 1.0, 305, "nohead/y", "f16").to(dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, 4, n_max))
+    for _ in range(2):
+        dv.dv_sparse_attn(y, Wqkv.to(dev), Wo.to(dev), kv, pos, idx, cnt, 0.125, out, ws,
+                          accumulate=accumulate)
+        assert dv.dv_check(ws)[0] == 0
+        assert torch.equal(out, base if accumulate else torch.zeros_like(base))
+    assert torch.equal(kv.X[0, 5], y[0])
+    assert int(kv.valid[0, :, 5].sum()) == 0
+
+
+def test_out_of_range_head_is_skipped_and_reported():
+    """A head index outside [0, h) adds nothing and is reported; the valid
+    heads of the list are still attended and projected."""
+    B, d, h, d_h, n_max = 1, 1024, 8, 128, 48
+    Wqkv, Wo = _layer("badhead", d, h, d_h, "f16", None)
+    dev = "cuda"
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    idx = torch.tensor([[1, h + 5, 6]], dtype=torch.int32, device=dev)
+    cnt = torch.tensor([3], dtype=torch.int32, device=dev)
+    y = draw((B, d), 1.0, 306, "badhead/y", "f16")
+    out = torch.zeros(B, d, device=dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, 3, n_max))
+    dv.dv_sparse_attn(y.to(dev), Wqkv.to(dev), Wo.to(dev), kv, pos, idx, cnt, 0.125, out, ws)
+    st, info = dv.dv_check(ws)
+    assert st == 5 and info == h + 5      # DV_ERR_INDEX_RANGE
+    c = oracle.KVCache.empty(h, n_max, d_h, d, "f16")
+    ref = oracle.sparse_attn(f64(y)[0], f64(Wqkv), f64(Wo), c, 0, [1, 6], 0.125)
+    assert_rel_l2(f64(out)[0], ref, "f16", "valid heads of the list")
 
 
 def test_position_outside_cache_is_reported():

@@ -21,6 +21,9 @@ CASES = [
     ("d136_f16",                  1, 136,   544,   "f16",  33),
     ("opt1.3b_f16",               1, 2048,  8192,  "f16",  410),
     ("opt13b_f16",                1, 5120,  20480, "f16",  1024),
+    ("d2560_f16_5chunk",          1, 2560,  10240, "f16",  301),
+    ("f32_d1200_5chunk_ragged",   1, 1200,  4800,  "f32",  97),
+    ("batch3_f16_d5120",          3, 5120,  20480, "f16",  555),
     ("opt30b_bf16",               1, 7168,  28672, "bf16", 1434),
     ("opt30b_bf16_half",          1, 7168,  28672, "bf16", 14336),
     ("opt175b_f16",               1, 12288, 49152, "f16",  2458),

@@ -147,3 +147,35 @@ def test_lookahead_on_side_stream_matches_predict():
     torch.cuda.synchronize()
     assert out.cpu().numpy()[0].tolist() == ref[0][0].tolist()
     assert int(cnt.item()) == 205
+
+
+#        name          N     distinct  scale  k
+TIES = [
+    ("dup3",          2100, 700,      1.0,   150),   # ties inside the cut's bin (direct ranking)
+    ("dup512",        4096, 8,        1.0,   1000),  # 512 equal keys per value (refinement path)
+    ("constant",      1000, 1,        0.0,   300),   # every score exactly 0.5
+    ("saturated",     4096, 4096,     300.0, 100),   # hundreds of scores exactly 1.0f
+]
+
+
+@pytest.mark.parametrize("case", TIES, ids=[c[0] for c in TIES])
+def test_topk_ties_resolved_by_index(case):
+    """Duplicated P2 rows give bit-identical scores (every row is reduced in
+    the same order), so the list must take equal scores lowest index first,
+    through both the direct ranking of the cut's bin and the refinement."""
+    name, N, distinct, scale, k = case
+    d, r = 512, 128
+    y = draw((1, d), 1.0, 107, name + "/y", "f16")
+    P1t = draw((r, d), d ** -0.5, 107, name + "/P1", "f16")
+    base = draw((distinct, r), r ** -0.5, 107, name + "/P2", "f32") * scale
+    P2t = base.repeat((N + distinct - 1) // distinct, 1)[:N]
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(7))
+    P2t = P2t[perm].to(torch.float16)
+    idx, cnt, s = _run(y, [(P1t, P2t, "topk", k, 0.5, k)], "f16")[0]
+    g = idx[0, : int(cnt[0])]
+    assert int(cnt[0]) == k
+    assert topk_list_is_valid(g, s[0], k)
+    if name == "constant":
+        assert g.tolist() == list(range(k))
+    if name == "saturated":
+        assert int(np.sum(s[0] == 1.0)) > 2 * k   # the cut lies among exact ties

@@ -96,3 +96,5 @@ def test_opt13b_width_two_layers():
     w = Workload("opt13b_2l", 3, d=5120, h=40, d_h=128, N=20480, r=1024, dtype="f16", layers=2,
                  n_prompt=1024, n_gen=3)
     assert _run_stack(w, steps=3) >= 1
+
+
