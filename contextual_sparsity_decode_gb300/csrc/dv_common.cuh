@@ -133,6 +133,21 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* tmp, int* total)
 // are visible, so only data the predecessor does not write may be read
 // before it.  grid_dep_launch() lets the successor start early.  Both are
 // no-ops for kernels launched the ordinary way.
+// Per-thread asynchronous 16-byte global -> shared copies (through L2), in
+// commit groups; wait_group<N> returns when at most N of the thread's groups
+// are still in flight, and the thread then sees its own copied data.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -176,6 +176,129 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
   if (n == 0) after_last_fma();
 }
 
+// Single-pass rows (every thread holds all of its chunks of the CTA's rows):
+// the same products as qkv_entries, pipelined for long entry lists (KV
+// repair of a head skipped for many steps).  Each thread copies its own
+// chunks of the vectors of the next `stages - 1` groups into shared memory
+// (cp.async, no registers held), so those loads are in flight while the
+// current group is multiplied; the cross-warp sums run once per kGB groups
+// (one barrier pair per 2 x kGB vectors instead of per 2).  The current
+// token of a batch-1 call comes from registers (ycur) as before.
+constexpr int kGB = 4;  // groups per cross-warp reduction
+
+// Staging depth of qkv_entries_pipe (used with 3 chunks per thread): 3
+// groups, 72 KB of shared memory, so two CTAs still fit on an SM.
+__host__ __device__ constexpr int qkv_stages(int qc) { return qc == 3 ? 3 : 2; }
+__host__ __device__ constexpr int qkv_stage_bytes(int qc) { return qkv_stages(qc) * kNE * qc * 256 * 16; }
+
+template <int S>
+__device__ __forceinline__ void cp_async_wait_stages() {
+  cp_async_wait<S - 1>();
+}
+
+template <typename T, int kQC, int kStages, typename F>
+__device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4 (&w)[kQR][kQC], int tl,
+                                 int m, int tbase, int i, int u, float (&redb)[8][kGB][kQR][kNE],
+                                 uint4* xs, const uint4 (&ycur)[kQC], bool ycur_ok, F&& after_last_fma) {
+  constexpr int V = Elem<T>::kVec;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tpr = 1 << tl, RS = 256 >> tl, tt = tid & (tpr - 1);
+  const int C = a.d / V;
+  const T* y = static_cast<const T*>(a.y);
+  const T* X = static_cast<const T*>(a.X);
+  const int ng = (n + kNE - 1) / kNE;
+  // slot of (stage, entry, chunk) for this thread: consecutive threads take
+  // consecutive 16-byte words (no bank conflicts)
+  auto slot = [&](int st, int e, int j) { return xs + ((st * kNE + e) * kQC + j) * 256 + tid; };
+  auto issue = [&](int g) {
+    if (g < ng) {
+      const int st = g % kStages;
+#pragma unroll
+      for (int e = 0; e < kNE; ++e) {
+        const int idx = g * kNE + e;
+        if (idx >= n) break;
+        const int en = ent[idx];
+        if ((en & kCur) && ycur_ok) continue;
+        const int b = (en >> 20) & 1023, jp = en & 0xfffff;
+        const T* vec = (en & kCur) ? y + (size_t)b * a.d : X + ((size_t)b * a.n_max + jp) * a.d;
+#pragma unroll
+        for (int j = 0; j < kQC; ++j) {
+          const int c = tt + j * tpr;
+          if (c < C) cp_async16(slot(st, e, j), vec + (size_t)c * V);
+        }
+      }
+    }
+    cp_async_commit();  // one group per call, empty or not, so the counting stays uniform
+  };
+#pragma unroll
+  for (int g = 0; g < kStages - 1; ++g) issue(g);
+  for (int gb0 = 0; gb0 < ng; gb0 += kGB) {
+    const int gbn = min(kGB, ng - gb0);
+    for (int q = 0; q < gbn; ++q) {
+      const int g = gb0 + q;
+      issue(g + kStages - 1);
+      cp_async_wait_stages<kStages>();  // group g has landed (for this thread)
+      const int st = g % kStages;
+      float acc[kQR][kNE];
+#pragma unroll
+      for (int k = 0; k < kQR; ++k)
+#pragma unroll
+        for (int e = 0; e < kNE; ++e) acc[k][e] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kQC; ++j) {
+        const int c = tt + j * tpr;
+        if (c >= C) break;
+#pragma unroll
+        for (int e = 0; e < kNE; ++e) {
+          const int idx = g * kNE + e;
+          if (idx >= n) break;
+          float xf[V];
+          if ((ent[idx] & kCur) && ycur_ok) unpack<T>(ycur[j], xf);
+          else unpack<T>(*slot(st, e, j), xf);
+#pragma unroll
+          for (int k = 0; k < kQR; ++k) {
+            float wf[V];
+            unpack<T>(w[k][j], wf);
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[k][e] = fmaf(wf[v], xf[v], acc[k][e]);
+          }
+        }
+      }
+      if (g == ng - 1) after_last_fma();
+#pragma unroll
+      for (int k = 0; k < kQR; ++k)
+#pragma unroll
+        for (int e = 0; e < kNE; ++e) {
+          const float z = warp_sum(acc[k][e]);
+          if (lane == 0) redb[wid][q][k][e] = z;
+        }
+    }
+    __syncthreads();
+    const int nw = tpr >> 5;
+    const int per_g = RS * kQR * kNE;
+    for (int o = tid; o < per_g * gbn; o += 256) {
+      const int q = o / per_g, r = o - q * per_g;
+      const int sl = r / (kQR * kNE), k = (r / kNE) % kQR, e = r % kNE;
+      const int idx = (gb0 + q) * kNE + e;
+      if (idx >= n) continue;
+      float z = 0.f;
+      for (int x = 0; x < nw; ++x) z += redb[sl * nw + x][q][k][e];
+      const int en = ent[idx];
+      const int b = (en >> 20) & 1023, jp = en & 0xfffff;
+      const int t = tbase + sl * kQR + k;
+      if (m == 0) {
+        a.q[((size_t)b * a.capU + u) * a.d_h + t] = z;
+      } else {
+        T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
+        dst[(((size_t)b * a.h + i) * a.n_max + jp) * a.d_h + t] = Elem<T>::from_f(z);
+      }
+    }
+    __syncthreads();  // redb is rewritten by the next batch
+  }
+  if (n == 0) after_last_fma();
+  cp_async_wait<0>();  // nothing of this call is left in flight
+}
+
 // Persistent over tiles: CTA b takes tiles b, b + G, ... (a tile = rpc rows of
 // one selected head's W^Q, W^K or W^V block).  The next tile's weights (and,
 // batch 1, its valid flags) are requested right after the current tile's
@@ -186,7 +309,11 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   __shared__ int ent[kWin];
   __shared__ int n_ent;
   __shared__ float red[8][kQR][kNE];
+  __shared__ float redb[8][kGB][kQR][kNE];
   __shared__ int U_s[1024];
+  extern __shared__ uint4 xs_dyn[];  // single-pass rows: staged vector chunks (qkv_entries_pipe)
+  constexpr int kStg = qkv_stages(kQC);
+  constexpr bool kPipe = kQC == 3;   // with 4 chunks the staging loop would spill
   const int tid = threadIdx.x;
   const int tpr = 1 << tl, RS = 256 >> tl, slot = tid >> tl, tt = tid & (tpr - 1);
   const int rpc = RS * kQR;
@@ -277,9 +404,13 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
     }
     __syncthreads();
     const int n_first = n_ent;
-    qkv_entries<T, kQC>(a, ent, n_first, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok, [&]() {
+    auto hook = [&]() {
       if (!(m > 0 && !fast_scan) && tn < ntiles) fetch(tn);
-    });
+    };
+    if (kPipe && one_pass)
+      qkv_entries_pipe<T, kQC, kStg>(a, ent, n_first, w, tl, m, tbase, i, u, redb, xs_dyn, ycur, ycur_ok, hook);
+    else
+      qkv_entries<T, kQC>(a, ent, n_first, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok, hook);
     if (m > 0 && !fast_scan) {
       // general path (batch > 1 or pos > 4096): windows of 4096 positions
       for (int b = 0; b < a.B; ++b) {
@@ -304,7 +435,11 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
             if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0) ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
           }
           __syncthreads();
-          qkv_entries<T, kQC>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false, []() {});
+          if (kPipe && one_pass)
+            qkv_entries_pipe<T, kQC, kStg>(a, ent, n_ent, w, tl, m, tbase, i, u, redb, xs_dyn, ycur, false,
+                                           []() {});
+          else
+            qkv_entries<T, kQC>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false, []() {});
         }
       }
       if (tn < ntiles) fetch(tn);
@@ -763,10 +898,17 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   // three chunks per thread when a row fits (fewer registers), else four
   const int pdl = (launch_overlap() > 0 && a.B == 1) ? 1 : 0;
   cudaError_t e;
-  if (a.d / Elem<T>::kVec <= (1 << tl) * 3)
-    e = launch_k(attn_qkv_kernel<T, 3>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
-  else
+  // single-pass rows stage their vectors in dynamic shared memory
+  const int C = a.d / Elem<T>::kVec;
+  if (C <= (1 << tl) * 3) {
+    const size_t smem = qkv_stage_bytes(3);
+    static const bool attr3 = cudaFuncSetAttribute(attn_qkv_kernel<T, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem) == cudaSuccess;
+    if (!attr3) return cudaErrorInvalidConfiguration;
+    e = launch_k(attn_qkv_kernel<T, 3>, dim3(grid), dim3(256), smem, stream, pdl != 0, 1, a, RG, tl, pdl);
+  } else {
     e = launch_k(attn_qkv_kernel<T, 4>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
+  }
   if (e != cudaSuccess) return e;
   // 2. split-KV softmax, one cluster per (row, head), cache bookkeeping
   e = launch_decode<T>(a, stream);
