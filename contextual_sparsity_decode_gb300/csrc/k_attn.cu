@@ -184,7 +184,7 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
 // current group is multiplied; the cross-warp sums run once per kGB groups
 // (one barrier pair per 2 x kGB vectors instead of per 2).  The current
 // token of a batch-1 call comes from registers (ycur) as before.
-constexpr int kGB = 4;  // groups per cross-warp reduction
+constexpr int kGB = 8;  // groups per cross-warp reduction
 
 // Staging depth of qkv_entries_pipe (used with 3 chunks per thread): 3
 // groups, 72 KB of shared memory, so two CTAs still fit on an SM.
