@@ -149,7 +149,7 @@ struct SelArgs {
 
 constexpr int kSelThreads = 1024;
 constexpr int kBins = 4096;  // histogram bins per refinement level (12 bits)
-constexpr int kSelLoads = 16;  // score loads in flight per thread
+constexpr int kSelLoads = 24;  // score loads in flight per thread (one round for N <= 24576)
 constexpr int kCand = 256;     // keys ranked directly in the cut's bin, at most
 
 // One CTA per (predictor, batch row).  The row's scores are staged in shared
