@@ -76,6 +76,7 @@ struct MlpWs {
   uint16_t* act_hi;
   uint16_t* act_lo;
   float* act;
+  int32_t* ctr;
 };
 MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   MlpWs w{};
@@ -83,6 +84,7 @@ MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   w.U = c.take<int32_t>((size_t)N);
   w.U_count = c.take<int32_t>(4);
   w.member = c.take<uint32_t>((size_t)B * ((N + 31) / 32));
+  if (B == 1) w.ctr = c.take<int32_t>(8);
   if (B >= kTcMinBatch) {
     w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(N));
     w.act_lo = c.take<uint16_t>((size_t)32 * tc_act_cols(N));
@@ -302,7 +304,7 @@ dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, con
   L.y = y; L.B = B; L.d = d; L.N = N; L.W1n = W1n; L.W2n = W2n;
   L.idx = idx; L.cap = cap; L.count = count; L.out = out; L.accumulate = accumulate ? 1 : 0;
   L.U = w.U; L.U_count = w.U_count; L.member = w.member;
-  L.act_hi = w.act_hi; L.act_lo = w.act_lo; L.act = w.act;
+  L.act_hi = w.act_hi; L.act_lo = w.act_lo; L.act = w.act; L.ctr = w.ctr;
   cudaError_t e = launch_sparse_mlp(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);
 }

@@ -84,6 +84,8 @@ struct MlpLaunch {
   void* act_hi; void* act_lo;
   // CUDA-core path: fp32 activations [B][cap] (B == 1) or [B][mlp_union_cap]
   float* act;
+  // batch 1: arrival counters of the one-launch MLP (zero between calls)
+  int* ctr;
 };
 
 // Room for the batch union of B lists of up to `cap` neurons out of N.

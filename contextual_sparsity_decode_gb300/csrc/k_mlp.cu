@@ -5,23 +5,25 @@
 //
 // W^1 and W^2 are stored neuron-major (row j = neuron j's d weights,
 // 16-byte aligned), so every selected neuron is two contiguous rows
-// ("Memory coalescing", §3.3).  Two launches:
-//   mlp_up        a_b[u] = ReLU(W^1[list[u]] . y_b) (x the row's membership
+// ("Memory coalescing", §3.3).  Two steps:
+//   up            a_b[u] = ReLU(W^1[list[u]] . y_b) (x the row's membership
 //                 mask when B > 1), a gathered row-dot: a CTA holds a tile of
 //                 selected rows and every thread issues all of its row loads
 //                 before using any (same tiling as the predictor GEMV);
-//   rows_combine  out_b (+)= sum_u a_b[u] W^2[list[u]], column-sliced with one
-//                 writer per output element (k_rows.cu).
+//   combine       out_b (+)= sum_u a_b[u] W^2[list[u]], column-sliced with one
+//                 writer per output element (rows_combine.cuh).
+// At batch 1 both run in one launch (mlp_fused_kernel) when its grid fits
+// on the GPU at once; otherwise as mlp_up_kernel + rows_combine_kernel.
 // Batches of 8+ rows in a 16-bit type use the tcgen05 path (k_mlp_tc.cu).
 
-#include "dv_kernels.h"
+#include "rows_combine.cuh"
 
 namespace dv {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kC = 4;   // 16-byte chunks per thread per pass over a row
-constexpr int kR = 3;   // rows per thread group
+constexpr int kUpC = 4;   // 16-byte chunks per thread per pass over a row
+constexpr int kUpR = 3;   // rows per thread group
 
 struct UpArgs {
   const void* y;
@@ -38,21 +40,22 @@ struct UpArgs {
   int pdl;                    // launched with overlap: y is read after grid_dep_wait()
 };
 
-int up_tpr_log2(int chunks) {
+int up_tpr_log2(int chunks, int kC) {
   int l = 5;
   while (l < 8 && (1 << l) * kC < chunks) ++l;
   return l;
 }
 
-template <typename T, int BT>
-__global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
+// One CTA (row tile bx) of the up-projection.
+template <typename T, int BT, int kC, int kR>
+__device__ __forceinline__ void mlp_up_block(const UpArgs& a, int bx) {
   constexpr int V = Elem<T>::kVec;
   __shared__ float red[kThreads / 32][kR][BT];
   __shared__ int nid_s[kThreads / 32 * kR];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int tpr = 1 << a.tl, RS = kThreads >> a.tl;
   const int slot = tid >> a.tl, tt = tid & (tpr - 1);
-  const int row0 = (blockIdx.x * RS + slot) * kR;  // positions in the list
+  const int row0 = (bx * RS + slot) * kR;  // positions in the list
   const int C = a.d / V;
   if (!a.pdl) grid_dep_launch();  // the down-projection may start loading its rows
   const int nb = min(BT, a.B - a.b0);
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
   const int nw = tpr >> 5;
   for (int e = tid; e < RS * kR * BT; e += kThreads) {
     const int sl = e / (kR * BT), k = (e / BT) % kR, b = e % BT;
-    const int pos = (blockIdx.x * RS + sl) * kR + k;
+    const int pos = (bx * RS + sl) * kR + k;
     if (pos >= a.cap || b >= nb) continue;
     const int j = nid_s[sl * kR + k];
     float z = 0.f;
@@ -135,6 +138,58 @@ __global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
     else if (a.member && !bit_test(a.member + (size_t)(a.b0 + b) * a.words, j)) act = 0.f;
     a.act[(size_t)(a.b0 + b) * a.cap + pos] = act;
   }
+}
+
+template <typename T, int BT>
+__global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
+  mlp_up_block<T, BT, kUpC, kUpR>(a, (int)blockIdx.x);
+}
+
+// Batch 1, one launch for both products: CTAs [0, nA) compute activations
+// (mlp_up_block, 5 chunks x 4 rows per thread so that few CTAs hold all
+// selected rows), CTAs [nA, nA + nB) are the column blocks of the second
+// product (rows_combine_block).  A down-projection CTA requests its W^2 rows
+// first and then waits for the nA arrivals on ctr[0].  The host launches
+// this kernel only when the whole grid fits on the GPU at once, so every CTA
+// can be resident together and a waiting CTA never keeps an up-projection
+// CTA from starting (CTAs of other kernels on the SMs finish without waiting
+// for this one); up-projection CTAs also have the lower indices.  The wait is
+// bounded and reports DV_ERR_TIMEOUT.  ctr[1] counts the down-projection CTAs
+// past the wait; the last resets both counters for the next call (the
+// workspace starts zeroed).
+constexpr long long kFusedWaitCycles = 1ll << 31;  // ~1 s
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) mlp_fused_kernel(UpArgs u, CombineLaunch c, int nA, int* ctr) {
+  if ((int)blockIdx.x < nA) {
+    mlp_up_block<T, 1, 5, 4>(u, (int)blockIdx.x);
+    __syncthreads();  // this CTA's activations are written
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(ctr, 1);
+    }
+    return;
+  }
+  const int nB = (int)gridDim.x - nA;
+  rows_combine_block<T, 1>(c, 0, (int)blockIdx.x - nA, [&] {
+    grid_dep_wait();  // out was written by kernels before this one
+    grid_dep_launch();
+    if (threadIdx.x == 0) {
+      const long long t0 = clock64();
+      int seen = 0;
+      while ((seen = ld_acquire_gpu(ctr)) < nA) {
+        if (clock64() - t0 > kFusedWaitCycles) {
+          set_error(c.hdr, DV_ERR_TIMEOUT, seen);
+          break;
+        }
+      }
+      if (atomicAdd(ctr + 1, 1) == nB - 1) {  // every CTA of the grid has arrived at both counters
+        ctr[0] = 0;
+        ctr[1] = 0;
+      }
+    }
+    __syncthreads();
+  });
 }
 
 // Union of the rows' lists: ascending U, |U|, and per-row membership bitmaps.
@@ -191,8 +246,21 @@ cudaError_t launch_up(const UpArgs& a, int grid, cudaStream_t stream) {
   return launch_k(mlp_up_kernel<T, BT>, dim3(grid), dim3(kThreads), 0, stream, a.pdl != 0, 1, a);
 }
 
+// Does the one-launch MLP's grid fit on the GPU at once?
 template <typename T>
-cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
+bool fused_fits(int grid, int num_sms) {
+  static int per_sm = -1;
+  if (per_sm < 0) {
+    int n = 0;
+    per_sm = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mlp_fused_kernel<T>, kThreads, 0) == cudaSuccess
+                 ? n : 0;
+    (void)cudaGetLastError();
+  }
+  return (long long)per_sm * num_sms >= grid;
+}
+
+template <typename T>
+cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms, cudaStream_t stream) {
   UpArgs u{};
   u.y = L.y; u.W1n = L.W1n;
   u.B = L.B; u.d = L.d; u.N = L.N;
@@ -203,9 +271,26 @@ cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t s
   } else {
     u.list = L.U; u.list_count = L.U_count; u.member = L.member; u.cap = mlp_union_cap(L.B, L.N, L.cap);
   }
-  u.tl = up_tpr_log2(L.d / Elem<T>::kVec);
   u.pdl = (launch_overlap() > 0 && L.B == 1) ? 1 : 0;
-  const int rpc = (kThreads >> u.tl) * kR;
+  CombineLaunch c{};
+  c.W = L.W2n; c.d = L.d;
+  c.units = u.list; c.n_units = u.list_count; c.cap_units = u.cap; c.rpu = 1; c.n_rows_units = L.N;
+  c.coef = L.act; c.coef_stride = (size_t)u.cap;
+  c.member = nullptr; c.words = 0;  // the activations already carry the masks
+  c.B = L.B; c.out = L.out; c.accumulate = L.accumulate; c.hdr = hdr;
+  const int C = L.d / Elem<T>::kVec;
+  if (L.B == 1 && L.ctr) {  // one launch for both products when its grid fits at once
+    UpArgs f = u;
+    f.tl = up_tpr_log2(C, 5);
+    const int rpcf = (kThreads >> f.tl) * 4;
+    const int nA = (f.cap + rpcf - 1) / rpcf;
+    const int nB = (C + kRcCW - 1) / kRcCW;
+    if (fused_fits<T>(nA + nB, num_sms))
+      return launch_k(mlp_fused_kernel<T>, dim3(nA + nB), dim3(kThreads), 0, stream, f.pdl != 0, 1, f, c,
+                      nA, L.ctr);
+  }
+  u.tl = up_tpr_log2(C, kUpC);
+  const int rpc = (kThreads >> u.tl) * kUpR;
   const int grid = (u.cap + rpc - 1) / rpc;
   for (int b0 = 0; b0 < L.B;) {
     const int nb = L.B - b0;
@@ -220,12 +305,6 @@ cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t s
     if (e != cudaSuccess) return e;
     b0 += bt;
   }
-  CombineLaunch c{};
-  c.W = L.W2n; c.d = L.d;
-  c.units = u.list; c.n_units = u.list_count; c.cap_units = u.cap; c.rpu = 1; c.n_rows_units = L.N;
-  c.coef = L.act; c.coef_stride = (size_t)u.cap;
-  c.member = nullptr; c.words = 0;  // the activations already carry the masks
-  c.B = L.B; c.out = L.out; c.accumulate = L.accumulate; c.hdr = hdr;
   return launch_rows_combine(c, dt, stream);
 }
 
@@ -246,7 +325,6 @@ cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int 
 
 cudaError_t launch_sparse_mlp(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms,
                               cudaStream_t stream) {
-  (void)num_sms;
   cudaError_t e = cudaSuccess;
   const bool tc = L.B > 1 && tc_mlp_supported(L.B, L.d, dt);
   if (!L.accumulate && tc) {  // the tensor-core path adds into out with atomics
@@ -260,9 +338,9 @@ cudaError_t launch_sparse_mlp(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, in
   }
   if (tc) return launch_sparse_mlp_tc(L, dt, hdr, stream);
   switch (dt) {
-    case DV_F32: return mlp_t<float>(L, dt, hdr, stream);
-    case DV_F16: return mlp_t<__half>(L, dt, hdr, stream);
-    case DV_BF16: return mlp_t<__nv_bfloat16>(L, dt, hdr, stream);
+    case DV_F32: return mlp_t<float>(L, dt, hdr, num_sms, stream);
+    case DV_F16: return mlp_t<__half>(L, dt, hdr, num_sms, stream);
+    case DV_BF16: return mlp_t<__nv_bfloat16>(L, dt, hdr, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -143,3 +143,38 @@ def test_batch_rows_use_their_own_sets():
     for b in range(4):
         one, _, _ = _run(y[b:b + 1], W1n, W2n, [sets[b]], k)
         assert np.allclose(out[b], one[0], rtol=1e-5, atol=1e-6)
+
+
+def test_batch1_calls_share_one_workspace():
+    """At batch 1 both products run in one launch whose arrival counters live
+    in the workspace: consecutive calls on one workspace (different sets, an
+    empty one, accumulate on and off, an index outside [0, N)) each match
+    the oracle, and the counters are back at zero after each call."""
+    d, N, cap = 1024, 4096, 300
+    W1n, W2n = _weights("reuse", d, N, "f16")
+    dev = "cuda"
+    W1d, W2d = W1n.to(dev), W2n.to(dev)
+    ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(1, d, N, cap))
+    g = torch.Generator().manual_seed(11)
+    for step, k in enumerate([205, 0, 300, 1, 150, 40]):
+        y = draw((1, d), 1.0, 208, f"reuse/y{step}", "f16")
+        S = torch.sort(torch.randperm(N, generator=g)[:k]).values.to(torch.int32)
+        bad = step == 5
+        if bad:
+            S[-1] = N + 3
+        idx = torch.full((1, cap), -1, dtype=torch.int32)
+        idx[0, :k] = S
+        cnt = torch.tensor([k], dtype=torch.int32)
+        acc = step % 2 == 1
+        base = draw((1, d), 1.0, 208, f"reuse/base{step}", "f32")
+        out = base.clone().to(dev) if acc else torch.full((1, d), 55.0, device=dev)
+        dv.dv_sparse_mlp(y.to(dev), W1d, W2d, idx.to(dev), cnt.to(dev), out, ws, accumulate=acc)
+        st, info = dv.dv_check(ws)
+        assert (st, info) == ((5, N + 3) if bad else (0, 0)), (step, st, info)
+        got = f64(out)[0] - (f64(base)[0] if acc else 0.0)
+        kept = [j for j in S.tolist() if j < N]
+        if not kept:
+            assert np.all(got == 0.0)
+        else:
+            ref = oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), np.array(kept))
+            assert_rel_l2(got, ref, "f16", f"call {step}")
