@@ -195,6 +195,53 @@ def test_out_of_range_head_is_skipped_and_reported():
     assert_rel_l2(f64(out)[0], ref, "f16", "valid heads of the list")
 
 
+def test_repair_beyond_one_scan_window():
+    """Batch 1 at position 4500, past the 4096 positions the projection
+    kernel scans in one pass: skipped positions on both sides of the window
+    boundary are repaired (stale values planted there must not survive), and
+    the output matches the oracle."""
+    B, d, h, d_h, n_max, P = 1, 256, 4, 64, 4608, 4500
+    name = "longctx"
+    Wqkv, Wo = _layer(name, d, h, d_h, "f16", None)
+    dev = "cuda"
+    Wqkv_d, Wo_d = Wqkv.to(dev), Wo.to(dev)
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
+    Xp = draw((P, d), 1.0, 309, name + "/X", "f16")
+    kv.X[0, :P].copy_(Xp.to(dev))
+    pos = torch.tensor([P], dtype=torch.int32, device=dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, h, n_max))
+    dv.dv_kv_repair(kv, Wqkv_d, pos, torch.arange(h, dtype=torch.int32, device=dev)[None],
+                    torch.tensor([h], dtype=torch.int32, device=dev), ws)
+    assert dv.dv_check(ws)[0] == 0
+    g = torch.Generator().manual_seed(5)
+    miss = torch.cat([torch.randperm(P, generator=g)[:70], torch.tensor([4095, 4096, 4097, P - 1])])
+    miss = torch.unique(miss)
+    for i in (0, 2):
+        kv.valid[0, i, miss.to(dev)] = 0
+        kv.K[0, i, miss.to(dev)] = 7.0
+        kv.V[0, i, miss.to(dev)] = -7.0
+    cache = oracle.KVCache.empty(h, n_max, d_h, d, "f16")
+    cache.X[:P] = f64(Xp)
+    cache.K[:, :P] = f64(kv.K)[0, :, :P]
+    cache.V[:, :P] = f64(kv.V)[0, :, :P]
+    cache.valid[:, :P] = kv.valid[0, :, :P].cpu().numpy() == 1
+    y = draw((B, d), 1.0, 309, name + "/y", "f16")
+    S = [0, 2, 3]
+    out = torch.zeros(B, d, device=dev)
+    ws1 = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, 3, n_max))
+    dv.dv_sparse_attn(y.to(dev), Wqkv_d, Wo_d, kv, pos, torch.tensor([S], dtype=torch.int32, device=dev),
+                      torch.tensor([3], dtype=torch.int32, device=dev), 0.125, out, ws1)
+    assert dv.dv_check(ws1)[0] == 0
+    ref = oracle.sparse_attn(f64(y)[0], f64(Wqkv), f64(Wo), cache, P, S, 0.125)
+    assert_rel_l2(f64(out)[0], ref, "f16", "position 4500")
+    K, V, valid = f64(kv.K)[0], f64(kv.V)[0], kv.valid[0].cpu().numpy()
+    m = miss.numpy()
+    for i in (0, 2):
+        assert np.all(valid[i, : P + 1] == 1)
+        assert within_ulp_product(K[i, m], f64(Xp)[m], f64(Wqkv)[i, 1], "f16"), f"K head {i}"
+        assert within_ulp_product(V[i, m], f64(Xp)[m], f64(Wqkv)[i, 2], "f16"), f"V head {i}"
+
+
 def test_position_outside_cache_is_reported():
     B, d, h, d_h, n_max = 1, 128, 4, 64, 16
     Wqkv, Wo = _layer("pos", d, h, d_h, "f16", None)
