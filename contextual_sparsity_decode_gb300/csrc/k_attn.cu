@@ -10,12 +10,13 @@
 //                dots them with every vector that needs them: the current
 //                token(s) and, for K/V rows, the stored embeddings X[j] of
 //                positions whose K/V were skipped (fused repair, so a repair
-//                costs no extra weight traffic).
+//                costs no extra weight traffic).  Its last CTA also appends
+//                X[pos] and writes the valid column of pos.
 //   attn_decode  split-KV softmax: one thread-block cluster per (row, head),
 //                each CTA a share of the positions with every K/V load of a
 //                batch issued before the first use; partials are pushed into
 //                rank 0's shared memory and combined after one cluster barrier.
-//                Also appends X[pos] and updates the valid flags.
+//                Marks the repaired positions valid.
 //   rows_combine out += sum_i H_i W_i^O as a weighted sum of the selected
 //                heads' W^O rows, column-sliced so every output element has
 //                one writer (k_rows.cu).
@@ -343,6 +344,45 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   if (!pdl) load_ycur();
   const int nU = max(0, min(cnt_raw, a.capU));
   const int ntiles = nU * RG;
+  // Bookkeeping of this call's token (after the wait for y):
+  // X[b][p] = y_b and valid[b][.][p] = (head selected).  Nothing in this
+  // call reads X[p] or the valid column p (repairs and the decode kernel
+  // read positions < p only).
+  auto append = [&]() {
+    for (int b = 0; b < a.B; ++b) {
+      const int p = row_pos(a, b);
+      if (p < 0) {  // uniform in the CTA
+        if (tid == 0) set_error(a.hdr, DV_ERR_POSITION, a.pos[b]);
+        continue;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.y) + (size_t)b * a.d);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + ((size_t)b * a.n_max + p) * a.d);
+      for (int k0 = tid; k0 < C; k0 += 8 * 256) {  // 8 loads in flight, then 8 stores
+        uint4 t8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (k0 + q * 256 < C) t8[q] = ld_cached(src + k0 + q * 256);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (k0 + q * 256 < C) dst[k0 + q * 256] = t8[q];
+      }
+      for (int i = tid; i < a.h; i += 256) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
+      __syncthreads();
+      const int cnt = max(0, min(a.head_count[b], a.cap));
+      for (int e = tid; e < cnt; e += 256) {
+        const int i = a.head_idx[(size_t)b * a.cap + e];
+        if (i >= 0 && i < a.h) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 1;
+      }
+      __syncthreads();
+    }
+  };
+  // The last CTA has the fewest tiles (tiles are dealt round-robin), so it
+  // waits for y and appends before loading its first tile; nothing else is
+  // live in its registers then.
+  if ((int)blockIdx.x == G - 1) {
+    grid_dep_wait();
+    append();
+  }
   if ((int)blockIdx.x >= ntiles) return;  // uniform, before any barrier
   __syncthreads();
 
@@ -512,38 +552,6 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   const int CSd = (int)gridDim.x;  // the grid is one cluster wide
   const int rank = (int)cluster_ctarank();
   const int p = row_pos(a, b);
-  if (s == a.cap) {  // housekeeping of row b (rank 0 only): append X[p], reset the valid column
-    if (rank != 0) return;
-    grid_dep_wait();
-    if (p < 0) {
-      if (tid == 0) set_error(a.hdr, DV_ERR_POSITION, a.pos[b]);
-      return;
-    }
-    constexpr int V = Elem<T>::kVec;
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.y) + (size_t)b * a.d);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + ((size_t)b * a.n_max + p) * a.d);
-    for (int k0 = tid; k0 < a.d / V; k0 += 8 * kDecThreads) {  // 8 loads in flight, then 8 stores
-      uint4 t8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int k = k0 + q * kDecThreads;
-        if (k < a.d / V) t8[q] = __ldg(src + k);
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int k = k0 + q * kDecThreads;
-        if (k < a.d / V) dst[k] = t8[q];
-      }
-    }
-    for (int i = tid; i < a.h; i += kDecThreads) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
-    __syncthreads();
-    const int cnt = max(0, min(a.head_count[b], a.cap));
-    for (int e = tid; e < cnt; e += kDecThreads) {
-      const int i = a.head_idx[(size_t)b * a.cap + e];
-      if (i >= 0 && i < a.h) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 1;
-    }
-    return;
-  }
   // count and head index are independent loads (s < cap keeps the index in bounds)
   const int cnt_raw = a.head_count[b];
   const int i = a.head_idx[(size_t)b * a.cap + s];
@@ -592,7 +600,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   }
   const int u = a.slot_of ? a.slot_of[i] : s;
   float* Hrow = a.H + ((size_t)b * a.capU + u) * DH;
-  if (p < 0) {  // nothing to attend: H = 0 (the position error is reported by housekeeping)
+  if (p < 0) {  // nothing to attend: H = 0 (attn_qkv reports the position error)
     if (rank == 0)
       for (int t = tid; t < DH; t += kDecThreads) Hrow[t] = 0.f;
     return;
@@ -878,7 +886,7 @@ int decode_cluster_width() {
 template <typename T, int DH>
 cudaError_t launch_decode_dh(const AttnArgs& a, cudaStream_t stream) {
   const int cw = decode_cluster_width<T, DH>();
-  return launch_k(attn_decode_kernel<T, DH>, dim3(cw, a.cap + 1, a.B), dim3(kDecThreads), 0, stream, true, cw, a);
+  return launch_k(attn_decode_kernel<T, DH>, dim3(cw, a.cap, a.B), dim3(kDecThreads), 0, stream, true, cw, a);
 }
 
 template <typename T>
