@@ -535,7 +535,7 @@ template <> struct KvRaw<__nv_bfloat16, 2> : KvRaw16x2<__nv_bfloat16> {};
 // barrier rank 0 combines the CSd partials in rank order and writes H.
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kMaxCSd = 8;   // CTAs per decode cluster, at most
+constexpr int kMaxCSd = 16;  // CTAs per decode cluster, at most
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
@@ -856,36 +856,47 @@ template <> dv_dtype dtype_of<float>() { return DV_F32; }
 template <> dv_dtype dtype_of<__half>() { return DV_F16; }
 template <> dv_dtype dtype_of<__nv_bfloat16>() { return DV_BF16; }
 
-// Cluster width of the decode kernel: 8 CTAs (measured on the 40-layer
-// OPT-13B-shaped step: 45.0 us per layer against 45.9 with 16 and 48.1 with
-// 4 -- wider clusters wait longer for enough free SMs in one GPC, narrower
-// ones give each CTA several rounds of K/V loads), 4 where 8 cannot be
-// held.
+// Cluster width of the decode kernel: enough CTAs that every warp's share
+// of the positions fits one batch of kPW at the cache's largest position
+// (ceil(n_max / 128)), at least 8 and at most 16, as the GPU can hold such
+// clusters (else 8, else 4).  Measured on the 40-layer OPT-13B-shaped step
+// (n_max 1152): 9 CTAs 44.6 us per layer, 8 45.1, 10 44.9, 16 45.9, 4 48.1.
+// A CTA with one batch per warp needs no second dependent round of K/V
+// loads; wider clusters wait longer for room in one GPC.
 template <typename T, int DH>
-int decode_cluster_width() {
-  static int w = 0;
-  if (w == 0) {
-    w = 4;
+bool decode_width_fits(int w) {
+  static int fits[kMaxCSd + 1] = {0};  // 0 unknown, 1 yes, 2 no
+  if (w < 1 || w > kMaxCSd) return false;
+  if (fits[w] == 0) {
+    if (w > 8) (void)cudaFuncSetAttribute(attn_decode_kernel<T, DH>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(8, 1, 1);
+    cfg.gridDim = dim3(w, 1, 1);
     cfg.blockDim = dim3(kDecThreads);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 8;
+    at[0].val.clusterDim.x = w;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<T, DH>, &cfg) == cudaSuccess && n >= 1) w = 8;
+    fits[w] = cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<T, DH>, &cfg) == cudaSuccess && n >= 1 ? 1 : 2;
     (void)cudaGetLastError();
   }
-  return w;
+  return fits[w] == 1;
+}
+
+template <typename T, int DH>
+int decode_cluster_width(int n_max) {
+  constexpr int kPos = kDecWarps * 16;  // positions per CTA in one batch (kPW = 16)
+  const int want = min(kMaxCSd, max(8, (n_max + kPos - 1) / kPos));
+  if (decode_width_fits<T, DH>(want)) return want;
+  return decode_width_fits<T, DH>(8) ? 8 : 4;
 }
 
 template <typename T, int DH>
 cudaError_t launch_decode_dh(const AttnArgs& a, cudaStream_t stream) {
-  const int cw = decode_cluster_width<T, DH>();
+  const int cw = decode_cluster_width<T, DH>(a.n_max);
   return launch_k(attn_decode_kernel<T, DH>, dim3(cw, a.cap, a.B), dim3(kDecThreads), 0, stream, true, cw, a);
 }
 
