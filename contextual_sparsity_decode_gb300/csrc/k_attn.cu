@@ -913,7 +913,12 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   const int RG = 3 * a.d_h / ((256 >> tl) * kQR);
   if (a.capU > 1024) return cudaErrorInvalidValue;
   const int tiles = a.capU * RG;
-  const int grid = tiles < 2 * num_sms ? tiles : 2 * num_sms;  // two resident CTAs per SM
+  // two resident CTAs per SM at most; no more CTAs than the largest number
+  // of tiles per CTA needs (768 tiles on 304 slots take 3 rounds either way,
+  // and 256 CTAs leave slots for the decode kernel's CTAs to start early)
+  const int slots = 2 * num_sms;
+  const int rounds = (tiles + slots - 1) / slots;
+  const int grid = (tiles + rounds - 1) / rounds;
   // three chunks per thread when a row fits (fewer registers), else four
   const int pdl = (launch_overlap() > 0 && a.B == 1) ? 1 : 0;
   cudaError_t e;
