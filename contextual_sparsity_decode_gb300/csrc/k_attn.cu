@@ -915,10 +915,12 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   const int tiles = a.capU * RG;
   // two resident CTAs per SM at most; no more CTAs than the largest number
   // of tiles per CTA needs (768 tiles on 304 slots take 3 rounds either way,
-  // and 256 CTAs leave slots for the decode kernel's CTAs to start early)
+  // and 256 CTAs leave slots for the decode kernel's CTAs to start early),
+  // plus one so that the last CTA, which also appends the token, has a tile
+  // fewer than the most loaded ones
   const int slots = 2 * num_sms;
   const int rounds = (tiles + slots - 1) / slots;
-  const int grid = (tiles + rounds - 1) / rounds;
+  const int grid = min(slots, (tiles + rounds - 1) / rounds + 1);
   // three chunks per thread when a row fits (fewer registers), else four
   const int pdl = (launch_overlap() > 0 && a.B == 1) ? 1 : 0;
   cudaError_t e;
