@@ -54,9 +54,11 @@ __global__ void __launch_bounds__(kLnThreads) layernorm_kernel(const float* x, i
   __shared__ float red[kLnThreads / 32];
   const int b = blockIdx.x, tid = threadIdx.x;
   // Launched programmatically: the input is read only after the previous
-  // kernel has completed, so this is safe after any kernel.
+  // kernel has completed, so this is safe after any kernel.  A consumer
+  // launched with overlap may start at once and request its weights while
+  // the kernel before this one still runs (dv_set_launch_overlap).
+  grid_dep_launch();
   grid_dep_wait();
-  grid_dep_launch();  // a consumer launched with overlap may start its own loads
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)b * d);
   const int n4 = d / 4;
   float4 v[kLnVec];

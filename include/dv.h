@@ -264,7 +264,10 @@ dv_status dv_layernorm(const float* x, int B, int d, float eps,
  * counts, pos, the valid flags and the weights.  Enable it only when the
  * kernel issued just before each such call (on the same stream) writes none
  * of those -- true when that kernel is the dv_layernorm producing the call's
- * y, as in a pre-LN decoder.  Process-wide; returns the previous level. */
+ * y, as in a pre-LN decoder -- and neither does the kernel before that
+ * layernorm, which lets its consumer start at once (in a pre-LN decoder it
+ * is the previous block's dv_sparse_attn or dv_sparse_mlp).  Process-wide;
+ * returns the previous level. */
 int dv_set_launch_overlap(int level);
 
 /* pos[b] = pos[b] + 1, or `lo` when that reaches `hi` (decode loop). */
