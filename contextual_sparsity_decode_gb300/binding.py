@@ -36,7 +36,8 @@ EXPORTS = (
     "dv_predict_workspace_size", "dv_predict", "dv_lookahead", "dv_predict_static",
     "dv_sparse_mlp_workspace_size", "dv_sparse_mlp",
     "dv_sparse_attn_workspace_size", "dv_sparse_attn", "dv_kv_repair",
-    "dv_layernorm", "dv_positions_advance", "dv_set_launch_overlap",
+    "dv_layernorm", "dv_positions_advance", "dv_set_launch_overlap", "dv_set_wait_limit_ns",
+    "dv_kernel_launches",
 )
 
 
@@ -87,6 +88,8 @@ _SIGS = {
     "dv_layernorm": ([_vp, _c_int, _c_int, _c_float, _vp, _c_int, _vp], _c_int),
     "dv_positions_advance": ([_vp, _c_int, _c_int, _c_int, _vp], _c_int),
     "dv_set_launch_overlap": ([_c_int], _c_int),
+    "dv_set_wait_limit_ns": ([ctypes.c_longlong], ctypes.c_longlong),
+    "dv_kernel_launches": ([], ctypes.c_longlong),
 }
 
 
@@ -156,6 +159,12 @@ def _ok(st: int, where: str):
 
 def dv_version() -> int:
     return lib().dv_version()
+
+
+def dv_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far (captured
+    launches included)."""
+    return int(lib().dv_kernel_launches())
 
 
 def dv_status_str(st: int) -> str:
@@ -316,3 +325,10 @@ def dv_set_launch_overlap(level: int) -> int:
     """Process-wide launch policy (see dv_set_launch_overlap in dv.h);
     returns the previous level."""
     return int(lib().dv_set_launch_overlap(int(level)))
+
+
+def dv_set_wait_limit_ns(ns: int) -> int:
+    """Process-wide bound of the device-side waits in nanoseconds (see
+    dv_set_wait_limit_ns in dv.h; ns <= 0 restores one second); returns the
+    previous bound."""
+    return int(lib().dv_set_wait_limit_ns(int(ns)))

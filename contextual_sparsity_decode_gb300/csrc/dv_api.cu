@@ -13,21 +13,26 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
+}  // namespace
+
+namespace dv {
 dv_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
   return DV_ERR_CUDA;
 }
+}  // namespace dv
+
+namespace {
 
 int num_sms_current() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cache[dev] == 0) {
+  static PerDevice cache;
+  const int dev = current_device();
+  return cache.get(dev, [dev] {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
-  }
-  return cache[dev];
+    if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    return n;
+  });
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -198,6 +203,10 @@ int dv_last_cuda_error(void) { return g_last_cuda_error; }
 int dv_version(void) { return 100; }
 
 int dv_set_launch_overlap(int level) { return set_launch_overlap(level); }
+
+long long dv_set_wait_limit_ns(long long ns) { return set_wait_limit_ns(ns); }
+
+long long dv_kernel_launches(void) { return launches_total(); }
 
 dv_status dv_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!ws || ws_bytes < sizeof(WsHeader)) return DV_ERR_INVALID_ARG;

@@ -9,8 +9,30 @@
 #include <cuda_runtime.h>
 
 #include "dv_common.cuh"
+#include "per_device.h"
 
 namespace dv {
+
+// The current device id (-1 if it cannot be read): the key of PerDevice caches.
+inline int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  return dev;
+}
+
+// Bound of every device-side wait, in nanoseconds of %globaltimer
+// (dv_set_wait_limit_ns; default one second).  A wait that runs out records
+// DV_ERR_TIMEOUT in the workspace and the kernel unwinds.
+long long wait_limit_ns();
+long long set_wait_limit_ns(long long ns);
+
+// Record a failed CUDA call for dv_last_cuda_error() and return DV_ERR_CUDA.
+dv_status cuda_fail(cudaError_t e);
+
+// Kernels this library has enqueued in this process (dv_kernel_launches):
+// every launch site adds its launches once they are accepted.
+void count_launches(int n);
+long long launches_total();
 
 // Launch with an optional programmatic dependency on the previous kernel of
 // the stream (see grid_dep_wait / grid_dep_launch).  Used only between the
@@ -40,7 +62,9 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   }
   cfg.attrs = n ? at : nullptr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 // Launch policy (dv_set_launch_overlap): 1 lets the first kernel of a batch-1

@@ -10,7 +10,7 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+using dv::kMaxDevices;
 constexpr int kStaticMaxB = 4;
 constexpr int kStaticMaxR = 1024;
 constexpr int kStaticMaxN = 32768;
@@ -60,14 +60,16 @@ extern "C" dv_status dv_predict_static(const void* y, int B, int d, dv_dtype dt,
   // device current
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DV_ERR_CUDA;
+  if (e != cudaSuccess) return dv::cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return dv::cuda_fail(cudaErrorInvalidDevice);
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_addr[dev]) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_predict_scratch);
-      if (e != cudaSuccess || !p) return DV_ERR_CUDA;
+      if (e != cudaSuccess) return dv::cuda_fail(e);
+      if (!p) return dv::cuda_fail(cudaErrorInvalidSymbol);
       g_addr[dev] = p;
     }
     base = g_addr[dev];
@@ -89,7 +91,7 @@ extern "C" dv_status dv_predict_static(const void* y, int B, int d, dv_dtype dt,
   }
   if ((size_t)(cur - static_cast<char*>(base)) > kStaticBytes) return DV_ERR_WORKSPACE;
   e = cudaMemsetAsync(base, 0, sizeof(dv::WsHeader), stream);
-  if (e != cudaSuccess) return DV_ERR_CUDA;
+  if (e != cudaSuccess) return dv::cuda_fail(e);
   e = dv::launch_predict(y, B, d, dt, L, n_preds, static_cast<dv::WsHeader*>(base), stream);
-  return e == cudaSuccess ? DV_OK : DV_ERR_CUDA;
+  return e == cudaSuccess ? DV_OK : dv::cuda_fail(e);
 }

@@ -865,9 +865,10 @@ template <> dv_dtype dtype_of<__nv_bfloat16>() { return DV_BF16; }
 // loads; wider clusters wait longer for room in one GPC.
 template <typename T, int DH>
 bool decode_width_fits(int w) {
-  static int fits[kMaxCSd + 1] = {0};  // 0 unknown, 1 yes, 2 no
+  // per device and width: 1 yes, 2 no (the attribute and the answer belong to the device)
+  static PerDevice fits[kMaxCSd + 1];
   if (w < 1 || w > kMaxCSd) return false;
-  if (fits[w] == 0) {
+  return fits[w].get(current_device(), [w] {
     if (w > 8) (void)cudaFuncSetAttribute(attn_decode_kernel<T, DH>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(w, 1, 1);
@@ -880,10 +881,10 @@ bool decode_width_fits(int w) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    fits[w] = cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<T, DH>, &cfg) == cudaSuccess && n >= 1 ? 1 : 2;
+    const int r = cudaOccupancyMaxActiveClusters(&n, attn_decode_kernel<T, DH>, &cfg) == cudaSuccess && n >= 1 ? 1 : 2;
     (void)cudaGetLastError();
-  }
-  return fits[w] == 1;
+    return r;
+  }) == 1;
 }
 
 template <typename T, int DH>
@@ -928,9 +929,11 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   const int C = a.d / Elem<T>::kVec;
   if (C <= (1 << tl) * 3) {
     const size_t smem = qkv_stage_bytes(3);
-    static const bool attr3 = cudaFuncSetAttribute(attn_qkv_kernel<T, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem) == cudaSuccess;
-    if (!attr3) return cudaErrorInvalidConfiguration;
+    static PerDevice attr3;  // function attributes are per device
+    const cudaError_t ea = (cudaError_t)attr3.get(current_device(), [smem] {
+      return (int)cudaFuncSetAttribute(attn_qkv_kernel<T, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (ea != cudaSuccess) return ea;
     e = launch_k(attn_qkv_kernel<T, 3>, dim3(grid), dim3(256), smem, stream, pdl != 0, 1, a, RG, tl, pdl);
   } else {
     e = launch_k(attn_qkv_kernel<T, 4>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
@@ -958,7 +961,9 @@ cudaError_t repair_t(const AttnLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   mark_valid_kernel<<<dim3(a.cap, a.B), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(2);
+  return e;
 }
 
 }  // namespace

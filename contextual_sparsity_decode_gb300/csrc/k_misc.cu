@@ -102,10 +102,21 @@ __global__ void positions_kernel(int32_t* pos, int B, int lo, int hi) {
 
 namespace {
 std::atomic<int> g_launch_overlap{0};
+constexpr long long kDefaultWaitNs = 1000000000LL;  // one second
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<long long> g_launches{0};
 }
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+long long launches_total() { return g_launches.load(std::memory_order_relaxed); }
 
 int launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed); }
 int set_launch_overlap(int level) { return g_launch_overlap.exchange(level > 0 ? 1 : 0); }
+
+long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+long long set_wait_limit_ns(long long ns) {
+  return g_wait_ns.exchange(ns > 0 ? ns : kDefaultWaitNs);
+}
 
 cudaError_t launch_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtype dt,
                              cudaStream_t stream) {
@@ -125,7 +136,9 @@ cudaError_t launch_layernorm(const float* x, int B, int d, float eps, void* y, d
 
 cudaError_t launch_positions_advance(int32_t* pos, int B, int lo, int hi, cudaStream_t stream) {
   positions_kernel<<<(B + 127) / 128, 128, 0, stream>>>(pos, B, lo, hi);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 }  // namespace dv

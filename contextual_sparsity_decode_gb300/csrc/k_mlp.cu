@@ -153,14 +153,17 @@ __global__ void __launch_bounds__(kThreads) mlp_up_kernel(UpArgs a) {
 // this kernel only when the whole grid fits on the GPU at once, so every CTA
 // can be resident together and a waiting CTA never keeps an up-projection
 // CTA from starting (CTAs of other kernels on the SMs finish without waiting
-// for this one); up-projection CTAs also have the lower indices.  The wait is
-// bounded and reports DV_ERR_TIMEOUT.  ctr[1] counts the down-projection CTAs
-// past the wait; the last resets both counters for the next call (the
-// workspace starts zeroed).
-constexpr long long kFusedWaitCycles = 1ll << 31;  // ~1 s
-
+// for this one); up-projection CTAs also have the lower indices.
+//
+// The wait is bounded (wait_ns of the global timer) and reports
+// DV_ERR_TIMEOUT.  ctr[1] counts the down-projection CTAs past the wait; the
+// last one takes nA back off ctr[0] and nB off ctr[1] (subtraction, not a
+// reset, so an up-projection CTA that arrives after a timed-out wait still
+// brings ctr[0] back to zero for the next call).  Counts above nA cannot
+// occur in a zero-filled workspace and are reported as DV_ERR_WORKSPACE.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) mlp_fused_kernel(UpArgs u, CombineLaunch c, int nA, int* ctr) {
+__global__ void __launch_bounds__(kThreads)
+    mlp_fused_kernel(UpArgs u, CombineLaunch c, int nA, int* ctr, long long wait_ns) {
   if ((int)blockIdx.x < nA) {
     mlp_up_block<T, 1, 5, 4>(u, (int)blockIdx.x);
     __syncthreads();  // this CTA's activations are written
@@ -175,17 +178,18 @@ __global__ void __launch_bounds__(kThreads) mlp_fused_kernel(UpArgs u, CombineLa
     grid_dep_wait();  // out was written by kernels before this one
     grid_dep_launch();
     if (threadIdx.x == 0) {
-      const long long t0 = clock64();
+      const unsigned long long t0 = globaltimer_ns();
       int seen = 0;
       while ((seen = ld_acquire_gpu(ctr)) < nA) {
-        if (clock64() - t0 > kFusedWaitCycles) {
+        if ((long long)(globaltimer_ns() - t0) > wait_ns) {
           set_error(c.hdr, DV_ERR_TIMEOUT, seen);
           break;
         }
       }
-      if (atomicAdd(ctr + 1, 1) == nB - 1) {  // every CTA of the grid has arrived at both counters
-        ctr[0] = 0;
-        ctr[1] = 0;
+      if (seen > nA) set_error(c.hdr, DV_ERR_WORKSPACE, seen);
+      if (atomicAdd(ctr + 1, 1) == nB - 1) {  // every down-projection CTA is past the wait
+        atomicSub(ctr, nA);
+        atomicSub(ctr + 1, nB);
       }
     }
     __syncthreads();
@@ -246,17 +250,19 @@ cudaError_t launch_up(const UpArgs& a, int grid, cudaStream_t stream) {
   return launch_k(mlp_up_kernel<T, BT>, dim3(grid), dim3(kThreads), 0, stream, a.pdl != 0, 1, a);
 }
 
-// Does the one-launch MLP's grid fit on the GPU at once?
+// Does the one-launch MLP's grid fit on the GPU at once?  (CTAs per SM are
+// a property of the device, so the answer is cached per device.)
 template <typename T>
 bool fused_fits(int grid, int num_sms) {
-  static int per_sm = -1;
-  if (per_sm < 0) {
+  static PerDevice per_sm;
+  const int n_sm = per_sm.get(current_device(), [] {
     int n = 0;
-    per_sm = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mlp_fused_kernel<T>, kThreads, 0) == cudaSuccess
-                 ? n : 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mlp_fused_kernel<T>, kThreads, 0) != cudaSuccess)
+      n = 0;
     (void)cudaGetLastError();
-  }
-  return (long long)per_sm * num_sms >= grid;
+    return n;
+  });
+  return (long long)n_sm * num_sms >= grid;
 }
 
 template <typename T>
@@ -287,7 +293,7 @@ cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms, c
     const int nB = (C + kRcCW - 1) / kRcCW;
     if (fused_fits<T>(nA + nB, num_sms))
       return launch_k(mlp_fused_kernel<T>, dim3(nA + nB), dim3(kThreads), 0, stream, f.pdl != 0, 1, f, c,
-                      nA, L.ctr);
+                      nA, L.ctr, wait_limit_ns());
   }
   u.tl = up_tpr_log2(C, kUpC);
   const int rpc = (kThreads >> u.tl) * kUpR;
@@ -320,7 +326,9 @@ cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int 
                          WsHeader* hdr, cudaStream_t stream) {
   const size_t smem = (size_t)((N + 31) / 32) * sizeof(uint32_t);
   union_kernel<<<1, 1024, smem, stream>>>(idx, cap, count, B, N, U, U_count, member, slot_of, hdr);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 cudaError_t launch_sparse_mlp(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms,

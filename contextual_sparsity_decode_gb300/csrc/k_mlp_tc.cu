@@ -17,7 +17,11 @@
 //         a_lo (two MMAs per K step).  Split-K over U with fp32 atomics.
 // One elected thread issues TMA loads into a ring of shared-memory stages,
 // one elected thread issues the MMAs; every wait is bounded and reports
-// DV_ERR_TIMEOUT instead of hanging.
+// DV_ERR_TIMEOUT instead of hanging.  The pipeline waits use the caller's
+// limit (dv_set_wait_limit_ns); the waits that unwind a CTA -- for the MMAs
+// it issued and for the TMA copies still landing in its shared memory --
+// take at least kUnwindNs, so no CTA frees its tensor memory or exits with
+// tensor-core or copy work of its own still in flight.
 
 #include <cuda.h>
 
@@ -33,7 +37,7 @@ constexpr int kTM = 128;                 // tile rows (M)
 constexpr int kKB = 64;                  // K elements per stage (one 128-byte row)
 constexpr int kStages = 4;
 constexpr int kKChunk = 1024;            // union neurons per down-projection CTA
-constexpr long long kWaitLimit = 2000000000LL;  // about one second of cycles
+constexpr long long kUnwindNs = 2000000000LL;  // two seconds
 constexpr uint32_t kTmemCols = 32;
 
 struct UpArgs {
@@ -45,6 +49,7 @@ struct UpArgs {
   void* act_hi;
   void* act_lo;
   WsHeader* hdr;
+  long long wait_ns;
 };
 
 struct DownArgs {
@@ -53,6 +58,7 @@ struct DownArgs {
   int capU, B, d, N;
   float* out;
   WsHeader* hdr;
+  long long wait_ns;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -71,6 +77,7 @@ __global__ void __launch_bounds__(128, 1)
   __shared__ int flag_err;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
   const int cnt = max(0, min(*a.U_count, a.capU));
   const int u0 = blockIdx.x * kTM;
   if (u0 >= cnt) return;  // whole CTA, before any barrier or TMEM use
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0 && lane == 0) {  // TMA producer
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % kStages, it = kb / kStages;
-      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, kWaitLimit)) {
+      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 1);
         flag_err = 1;
         break;
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, false, false);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % kStages, it = kb / kStages;
-      if (!tc::mbar_wait(&full[s], it & 1, kWaitLimit)) {
+      if (!tc::mbar_wait(&full[s], it & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 2);
         flag_err = 1;
         break;
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncwarp();
 
   // epilogue: thread = accumulator row (neuron u0 + tid)
-  const bool ok = tc::mbar_wait(&done, 0, kWaitLimit);
+  const bool ok = tc::mbar_wait(&done, 0, unwind_ns);
   if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 3);
   __syncwarp();
   tc::fence_after_sync();
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(128, 1)
   // make sure no TMA write into this CTA's shared memory is still in flight
   if (tid == 0) {
     for (int kb = consumed; kb < issued; ++kb)
-      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, kWaitLimit)) break;
+      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, unwind_ns)) break;
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -194,6 +201,7 @@ __global__ void __launch_bounds__(128, 1)
   __shared__ int issued, consumed, flag_err;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
   const int cnt = max(0, min(*a.U_count, a.capU));
   const int c0 = blockIdx.x * kTM;
   const int k0 = blockIdx.y * kKChunk;
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0 && lane == 0) {  // TMA producer
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % kStages, it = kb / kStages;
-      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, kWaitLimit)) {
+      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 4);
         flag_err = 1;
         break;
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, /*A MN-major*/ true, false);
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % kStages, it = kb / kStages;
-      if (!tc::mbar_wait(&full[s], it & 1, kWaitLimit)) {
+      if (!tc::mbar_wait(&full[s], it & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 5);
         flag_err = 1;
         break;
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  const bool ok = tc::mbar_wait(&done, 0, kWaitLimit);
+  const bool ok = tc::mbar_wait(&done, 0, unwind_ns);
   if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 6);
   __syncwarp();
   tc::fence_after_sync();
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (tid == 0) {
     for (int kb = consumed; kb < issued; ++kb)
-      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, kWaitLimit)) break;
+      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, unwind_ns)) break;
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -347,25 +355,28 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const size_t smem_up = 1024 + kStages * (kTM * 128 + BP * 128);
   const size_t smem_dn = 1024 + kStages * (kKB * 256 + 2 * BP * 128);
-  static bool attr = false;
-  if (!attr) {
+  static PerDevice attr;  // function attributes are per device
+  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [&] {
     cudaError_t e = cudaFuncSetAttribute(mlp_tc_up_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem_up);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(mlp_tc_down_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_dn);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mlp_tc_down_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem_dn);
+    return (int)e;
+  });
+  if (ea != cudaSuccess) return ea;
   const int maxU = L.N < L.B * L.cap ? L.N : L.B * L.cap;
-  UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr};
+  UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr,
+            wait_limit_ns()};
   mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, 128, smem_up, stream>>>(mW1, mY, ua);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr};
+  DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr, wait_limit_ns()};
   dim3 g(L.d / kTM, (maxU + kKChunk - 1) / kKChunk);
   mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW2, mHi, mLo, da);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(2);
+  return e;
 }
 
 }  // namespace

@@ -430,13 +430,12 @@ cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_pr
     nmax = p.N[i] > nmax ? p.N[i] : nmax;
   }
   const size_t smem = (size_t)nmax * sizeof(uint32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t ea = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)(kSelectMaxN * sizeof(uint32_t)));
-    if (ea != cudaSuccess) return ea;
-    attr_set = true;
-  }
+  static PerDevice attr;  // function attributes are per device
+  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [] {
+    return (int)cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kSelectMaxN * sizeof(uint32_t)));
+  });
+  if (ea != cudaSuccess) return ea;
   return launch_k(select_kernel, dim3(B, n_preds), dim3(kSelThreads), smem, stream, true, 1, sa, hdr);
 }
 

@@ -39,12 +39,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity; gives up after `limit` cycles and
-// returns false (the caller records DV_ERR_TIMEOUT and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
-  const long long t0 = clock64();
+// Wait for the phase with the given parity; gives up after `limit_ns`
+// nanoseconds of the global timer and returns false (the caller records
+// DV_ERR_TIMEOUT and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
+  const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > limit) return false;
+    if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
   }
   return true;
 }

@@ -29,10 +29,15 @@ class SparseDecoder:
 
     layers: per layer a dict of weight tensors in the library layouts
             (Wqkv, Wo, W1n, W2n, PA1t, PA2t, PM1t, PM2t), all of one dtype.
+    trace:  keep a copy of the residual stream before layer 0 (r_in0) and
+            after every block of every layer (r_mid[l] after the attention,
+            r_out[l] after the MLP), so that each block can be checked on its
+            own inputs (plain device copies between the calls).
     """
 
     def __init__(self, layers: List[Dict[str, torch.Tensor]], B: int, n_max: int,
-                 k_heads: int, k_neurons: int, scale: float, eps: float = 1e-5):
+                 k_heads: int, k_neurons: int, scale: float, eps: float = 1e-5,
+                 trace: bool = False):
         W0 = layers[0]
         self.layers = layers
         self.L = len(layers)
@@ -53,8 +58,14 @@ class SparseDecoder:
         self.neur_idx = [torch.zeros(B, k_neurons, **i32) for _ in layers]
         self.neur_cnt = [torch.zeros(B, **i32) for _ in layers]
         self.y_a = [torch.zeros(B, d, dtype=self.dtype, device=dev) for _ in layers]
-        self.y_m = torch.zeros(B, d, dtype=self.dtype, device=dev)
+        self.y_m = [torch.zeros(B, d, dtype=self.dtype, device=dev) for _ in layers]
         self.r_stream = torch.zeros(B, d, dtype=torch.float32, device=dev)   # residual
+        self.trace = bool(trace)
+        if self.trace:
+            f32 = dict(dtype=torch.float32, device=dev)
+            self.r_in0 = torch.zeros(B, d, **f32)
+            self.r_mid = [torch.zeros(B, d, **f32) for _ in layers]
+            self.r_out = [torch.zeros(B, d, **f32) for _ in layers]
         self.pos = torch.zeros(B, **i32)
         self.ws_pred_main = dv.workspace(dv.dv_predict_workspace_size(B, 2, self.r, self.N), dev)
         self.ws_pred_side = dv.workspace(dv.dv_predict_workspace_size(B, 2, self.r, self.N), dev)
@@ -70,6 +81,22 @@ class SparseDecoder:
         # around every call of it on the main stream)
         self.timed: Optional[str] = None
         self.t_ev: List[torch.cuda.Event] = []
+
+    def set_keep(self, k_heads: int, k_neurons: int):
+        """Change the number of heads and neurons kept per layer (new index
+        lists and block workspaces; the KV caches are kept).  Re-capture
+        the graph afterwards."""
+        dev, B = self.device, self.B
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.k_heads, self.k_neurons = k_heads, k_neurons
+        self.head_idx = [torch.zeros(B, k_heads, **i32) for _ in self.layers]
+        self.head_cnt = [torch.zeros(B, **i32) for _ in self.layers]
+        self.neur_idx = [torch.zeros(B, k_neurons, **i32) for _ in self.layers]
+        self.neur_cnt = [torch.zeros(B, **i32) for _ in self.layers]
+        self.ws_attn = dv.workspace(
+            dv.dv_sparse_attn_workspace_size(B, self.d, self.h, self.d_h, k_heads, self.n_max), dev)
+        self.ws_mlp = dv.workspace(dv.dv_sparse_mlp_workspace_size(B, self.d, self.N, k_neurons), dev)
+        self.graph = None
 
     # ------------------------------------------------------------------ pieces
     def predictors(self, l: int):
@@ -123,9 +150,13 @@ class SparseDecoder:
 
     def _step_ops(self):
         main = torch.cuda.current_stream()
+        if self.trace:
+            self.r_in0.copy_(self.r_stream)
         for l in range(self.L):
             W = self.layers[l]
+            self._time("ln")
             dv.dv_layernorm(self.r_stream, self.y_a[l], self.eps)
+            self._time("ln")
             if l == 0:
                 self._time("predict")
                 dv.dv_predict(self.y_a[0], self.predictors(0), self.ws_pred_main)
@@ -154,11 +185,17 @@ class SparseDecoder:
                               self.ws_attn, accumulate=True)
             dv.dv_set_launch_overlap(1)
             self._time("attn")
-            dv.dv_layernorm(self.r_stream, self.y_m, self.eps)
+            if self.trace:
+                self.r_mid[l].copy_(self.r_stream)
+            self._time("ln")
+            dv.dv_layernorm(self.r_stream, self.y_m[l], self.eps)
+            self._time("ln")
             self._time("mlp")
-            dv.dv_sparse_mlp(self.y_m, W["W1n"], W["W2n"], self.neur_idx[l], self.neur_cnt[l],
+            dv.dv_sparse_mlp(self.y_m[l], W["W1n"], W["W2n"], self.neur_idx[l], self.neur_cnt[l],
                              self.r_stream, self.ws_mlp, accumulate=True)
             self._time("mlp")
+            if self.trace:
+                self.r_out[l].copy_(self.r_stream)
 
     def capture(self, advance: Optional[tuple] = None):
         """Capture one token (optionally followed by pos advance (lo, hi))

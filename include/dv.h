@@ -35,8 +35,13 @@
  *  - Scratch space: each call takes a caller-owned device workspace of at
  *    least the size its *_workspace_size() query reports.  A workspace must
  *    be zero-filled once (dv_workspace_init) before its first use; the
- *    library leaves it reusable.  Calls that may run concurrently (e.g. the
- *    look-ahead predictor on a side stream) need distinct workspaces.
+ *    library leaves it reusable, also after a device wait has timed out
+ *    (DV_ERR_TIMEOUT): a late arrival still brings the workspace's counters
+ *    back to zero.  A workspace that was never zero-filled reports
+ *    DV_ERR_TIMEOUT or DV_ERR_WORKSPACE from dv_check; zero-fill it
+ *    (dv_workspace_init) before the next call.  Calls that may run
+ *    concurrently (e.g. the look-ahead predictor on a side stream) need
+ *    distinct workspaces.
  *  - Errors found on the host (bad arguments) are returned at once and
  *    nothing is launched.  Errors found on the device (an index outside
  *    [0, N), a count above cap, a position outside the cache) never trap:
@@ -119,6 +124,11 @@ const char* dv_status_str(dv_status s);
 int dv_last_cuda_error(void);
 /* Library version, e.g. 100 for 0.1.0. */
 int dv_version(void);
+/* Number of kernels the library has enqueued in this process so far,
+ * launches captured into a CUDA graph included (a diagnostic: the difference
+ * across the calls of one step is that step's kernel count).  No
+ * counterpart in the pages. */
+long long dv_kernel_launches(void);
 
 /* Zero-fill a workspace (once, before its first use). */
 dv_status dv_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -269,6 +279,16 @@ dv_status dv_layernorm(const float* x, int B, int d, float eps,
  * is the previous block's dv_sparse_attn or dv_sparse_mlp).  Process-wide;
  * returns the previous level. */
 int dv_set_launch_overlap(int level);
+
+/* Bound of every device-side wait (no counterpart in the pages): the
+ * one-launch MLP's wait for its up-projection CTAs and the tensor-core
+ * path's pipeline waits give up after `ns` nanoseconds of the GPU's global
+ * timer, record DV_ERR_TIMEOUT in the workspace (read it with dv_check) and
+ * unwind; the kernel still waits for its own tensor-core and copy work in
+ * flight before it exits.  ns <= 0 restores the default of one second.
+ * Read at launch (a captured graph keeps the value it was captured with);
+ * process-wide; returns the previous bound. */
+long long dv_set_wait_limit_ns(long long ns);
 
 /* pos[b] = pos[b] + 1, or `lo` when that reaches `hi` (decode loop). */
 dv_status dv_positions_advance(int32_t* pos, int B, int lo, int hi,
