@@ -312,7 +312,8 @@ def run_stack(args, w, B, rank, world, local, full_layers, with_e2e=True):
     dv.lib()
     layers = [layer_weights(w, l, device=dev) for l in range(w.layers)]
     scale = 1.0 / math.sqrt(w.d_h)
-    dec = SparseDecoder(layers, B, w.n_max, w.k_heads, w.k_neurons, scale)
+    n_cache = (w.n_max + 15) // 16 * 16  # the cache holds a multiple of 16 positions
+    dec = SparseDecoder(layers, B, n_cache, w.k_heads, w.k_neurons, scale)
     dec.prefill([torch.stack([embeddings(w, w.n_prompt, f"X{l}" if B == 1 else f"X{l}/{b}", device=dev)
                               for b in range(B)]) for l in range(w.layers)], w.n_prompt)
     dec.r_stream.copy_(residual_input(w, B, "r0", device=dev))

@@ -125,6 +125,13 @@ cudaError_t launch_sparse_mlp_tc(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
 cudaError_t launch_sparse_mlp(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
                               int num_sms, cudaStream_t stream);
 
+// Batch 1, streaming pass over the selected rows with bulk copies into a
+// shared-memory ring (k_stream.cu); adds into out with atomics.
+bool mlp_stream_supported(int d, dv_dtype dt);
+cudaError_t launch_mlp_stream(const void* y, int d, int N, const void* W1n, const void* W2n,
+                              const int32_t* list, const int32_t* count, int cap, dv_dtype dt, float* out,
+                              WsHeader* hdr, int num_sms, int pdl, cudaStream_t stream);
+
 // Union of per-row index lists: U ascending, U_count, member bitmaps and
 // (optional) slot_of[unit] = position of the unit in U.
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B,
@@ -152,6 +159,12 @@ cudaError_t launch_sparse_attn(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
                                int num_sms, cudaStream_t stream);
 cudaError_t launch_kv_repair(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
                              cudaStream_t stream);
+
+// Bulk K/V fill of the missing positions on the tensor cores (k_kv_tc.cu):
+// 16-bit storage, d_h 64 or 128.
+bool kv_tc_supported(int d, int d_h, dv_dtype dt);
+cudaError_t launch_kv_repair_tc(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
+                                cudaStream_t stream);
 
 // ---- weighted sum of selected rows, column-sliced (k_rows.cu) -----------------
 

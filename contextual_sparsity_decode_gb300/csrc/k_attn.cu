@@ -20,8 +20,9 @@
 //   rows_combine out += sum_i H_i W_i^O as a weighted sum of the selected
 //                heads' W^O rows, column-sliced so every output element has
 //                one writer (k_rows.cu).
-// The standalone repair (dv_kv_repair, e.g. a dense prefill) uses a tiled
-// CUDA-core GEMM over the missing positions instead.
+// The standalone repair (dv_kv_repair, e.g. a dense prefill) is a GEMM over
+// the missing positions: on the tensor cores for 16-bit storage
+// (k_kv_tc.cu), else the tiled CUDA-core GEMM below.
 
 #include "dv_kernels.h"
 
@@ -984,6 +985,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch& L, dv_dtype dt, WsHeader* hdr, 
 }
 
 cudaError_t launch_kv_repair(const AttnLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
+  if (kv_tc_supported(L.d, L.d_h, dt)) return launch_kv_repair_tc(L, dt, hdr, stream);
   switch (dt) {
     case DV_F32: return repair_t<float>(L, hdr, stream);
     case DV_F16: return repair_t<__half>(L, hdr, stream);

@@ -16,6 +16,8 @@
 // on the GPU at once; otherwise as mlp_up_kernel + rows_combine_kernel.
 // Batches of 8+ rows in a 16-bit type use the tcgen05 path (k_mlp_tc.cu).
 
+#include <cstdlib>
+
 #include "rows_combine.cuh"
 
 namespace dv {
@@ -265,6 +267,18 @@ bool fused_fits(int grid, int num_sms) {
   return (long long)n_sm * num_sms >= grid;
 }
 
+// Batch-1 path choice: the streaming pass for long rows.  DV_MLP_STREAM=1 or
+// 0 in the environment forces it on or off (measurement).
+bool use_stream(int d, dv_dtype dt) {
+  static const int forced = [] {
+    const char* e = getenv("DV_MLP_STREAM");
+    return e ? atoi(e) : -1;
+  }();
+  if (!mlp_stream_supported(d, dt)) return false;
+  if (forced >= 0) return forced != 0;
+  return (size_t)d * (dt == DV_F32 ? 4 : 2) >= 16384;
+}
+
 template <typename T>
 cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms, cudaStream_t stream) {
   UpArgs u{};
@@ -285,6 +299,14 @@ cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms, c
   c.member = nullptr; c.words = 0;  // the activations already carry the masks
   c.B = L.B; c.out = L.out; c.accumulate = L.accumulate; c.hdr = hdr;
   const int C = L.d / Elem<T>::kVec;
+  if (L.B == 1 && use_stream(L.d, dt)) {
+    if (!L.accumulate) {  // the streaming pass adds into out
+      cudaError_t e = cudaMemsetAsync(L.out, 0, (size_t)L.d * sizeof(float), stream);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_mlp_stream(L.y, L.d, L.N, L.W1n, L.W2n, L.idx, L.count, L.cap, dt, L.out, hdr, num_sms,
+                             u.pdl, stream);
+  }
   if (L.B == 1 && L.ctr) {  // one launch for both products when its grid fits at once
     UpArgs f = u;
     f.tl = up_tpr_log2(C, 5);

@@ -35,7 +35,12 @@ namespace {
 
 constexpr int kTM = 128;                 // tile rows (M)
 constexpr int kKB = 64;                  // K elements per stage (one 128-byte row)
-constexpr int kStages = 4;
+// Ring depths: a CTA keeps its whole ring in flight, and a 128-row tile
+// streams at most ~1/128 of the union per CTA, so the rings fill the shared
+// memory (up: 10 x 20 KB, down: 8 x 24 KB at 32 rows) to keep enough bytes
+// in flight per SM for HBM bandwidth.
+constexpr int kSU = 10;
+constexpr int kSD = 8;
 constexpr int kKChunk = 1024;            // union neurons per down-projection CTA
 constexpr long long kUnwindNs = 2000000000LL;  // two seconds
 constexpr uint32_t kTmemCols = 32;
@@ -71,7 +76,7 @@ __global__ void __launch_bounds__(128, 1)
                      UpArgs a) {
   constexpr uint32_t kABytes = kTM * 128, kBBytes = BP * 128;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint64_t full[kSU], empty[kSU], done;
   __shared__ uint32_t tmem_base;
   __shared__ int rows[kTM];
   __shared__ int flag_err;
@@ -84,7 +89,7 @@ __global__ void __launch_bounds__(128, 1)
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
+  uint8_t* sB = smem + kSU * kABytes;
 
   {
     int r = a.U[min(u0 + tid, cnt - 1)];
@@ -95,7 +100,7 @@ __global__ void __launch_bounds__(128, 1)
     rows[tid] = r;
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSU; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -115,8 +120,8 @@ __global__ void __launch_bounds__(128, 1)
 
   if (warp == 0 && lane == 0) {  // TMA producer
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages, it = kb / kStages;
-      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
+      const int s = kb % kSU, it = kb / kSU;
+      if (kb >= kSU && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 1);
         flag_err = 1;
         break;
@@ -134,7 +139,7 @@ __global__ void __launch_bounds__(128, 1)
     constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
     const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, false, false);
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages, it = kb / kStages;
+      const int s = kb % kSU, it = kb / kSU;
       if (!tc::mbar_wait(&full[s], it & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 2);
         flag_err = 1;
@@ -183,7 +188,7 @@ __global__ void __launch_bounds__(128, 1)
   // make sure no TMA write into this CTA's shared memory is still in flight
   if (tid == 0) {
     for (int kb = consumed; kb < issued; ++kb)
-      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, unwind_ns)) break;
+      if (!tc::mbar_wait(&full[kb % kSU], (kb / kSU) & 1, unwind_ns)) break;
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(128, 1)
                        const __grid_constant__ CUtensorMap mapLo, DownArgs a) {
   constexpr uint32_t kABytes = kKB * 256, kBBytes = BP * 128;  // A: 64 neurons x 128 columns
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kStages], empty[kStages], done;
+  __shared__ uint64_t full[kSD], empty[kSD], done;
   __shared__ uint32_t tmem_base;
   __shared__ int rows[kKChunk];
   __shared__ int issued, consumed, flag_err;
@@ -211,8 +216,8 @@ __global__ void __launch_bounds__(128, 1)
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
-  uint8_t* sH = smem + kStages * kABytes;
-  uint8_t* sL = sH + kStages * kBBytes;
+  uint8_t* sH = smem + kSD * kABytes;
+  uint8_t* sL = sH + kSD * kBBytes;
 
   for (int i = tid; i < nk * kKB; i += blockDim.x) {
     int r = a.U[min(k0 + i, cnt - 1)];
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(128, 1)
     rows[i] = r;
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSD; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -239,8 +244,8 @@ __global__ void __launch_bounds__(128, 1)
 
   if (warp == 0 && lane == 0) {  // TMA producer
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages, it = kb / kStages;
-      if (kb >= kStages && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
+      const int s = kb % kSD, it = kb / kSD;
+      if (kb >= kSD && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 4);
         flag_err = 1;
         break;
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(128, 1)
     constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
     const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, /*A MN-major*/ true, false);
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages, it = kb / kStages;
+      const int s = kb % kSD, it = kb / kSD;
       if (!tc::mbar_wait(&full[s], it & 1, a.wait_ns)) {
         set_error(a.hdr, DV_ERR_TIMEOUT, 5);
         flag_err = 1;
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (tid == 0) {
     for (int kb = consumed; kb < issued; ++kb)
-      if (!tc::mbar_wait(&full[kb % kStages], (kb / kStages) & 1, unwind_ns)) break;
+      if (!tc::mbar_wait(&full[kb % kSD], (kb / kSD) & 1, unwind_ns)) break;
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -353,8 +358,8 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
       !make_map(&mY, L.y, L.d, L.B, BP, bf16) || !make_map(&mHi, L.act_hi, Upad, BP, BP, bf16) ||
       !make_map(&mLo, L.act_lo, Upad, BP, BP, bf16))
     return cudaErrorInvalidValue;
-  const size_t smem_up = 1024 + kStages * (kTM * 128 + BP * 128);
-  const size_t smem_dn = 1024 + kStages * (kKB * 256 + 2 * BP * 128);
+  const size_t smem_up = 1024 + kSU * (kTM * 128 + BP * 128);
+  const size_t smem_dn = 1024 + kSD * (kKB * 256 + 2 * BP * 128);
   static PerDevice attr;  // function attributes are per device
   const cudaError_t ea = (cudaError_t)attr.get(current_device(), [&] {
     cudaError_t e = cudaFuncSetAttribute(mlp_tc_up_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
