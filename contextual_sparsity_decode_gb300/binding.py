@@ -37,7 +37,8 @@ EXPORTS = (
     "dv_sparse_mlp_workspace_size", "dv_sparse_mlp",
     "dv_sparse_attn_workspace_size", "dv_sparse_attn", "dv_kv_repair",
     "dv_layernorm", "dv_positions_advance", "dv_set_launch_overlap", "dv_set_wait_limit_ns",
-    "dv_kernel_launches",
+    "dv_kernel_launches", "dv_label_workspace_size", "dv_label_neurons", "dv_label_heads",
+    "dv_select_scores",
 )
 
 
@@ -90,6 +91,12 @@ _SIGS = {
     "dv_set_launch_overlap": ([_c_int], _c_int),
     "dv_set_wait_limit_ns": ([ctypes.c_longlong], ctypes.c_longlong),
     "dv_kernel_launches": ([], ctypes.c_longlong),
+    "dv_label_workspace_size": ([_c_int, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_sz)], _c_int),
+    "dv_label_neurons": ([_vp, _c_int, _c_int, _c_int, _vp, _c_int, _vp, _vp, _sz, _vp], _c_int),
+    "dv_label_heads": ([_vp, _c_int, _c_int, _c_int, _c_int, _vp, _c_float, _c_int, _vp, _vp, _sz, _vp],
+                       _c_int),
+    "dv_select_scores": ([_vp, _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _c_int, _vp, _vp, _sz, _vp],
+                         _c_int),
 }
 
 
@@ -306,6 +313,33 @@ def dv_kv_repair(kv: KV, Wqkv, pos, head_idx, head_count, ws, stream=None):
     _ok(lib().dv_kv_repair(ctypes.byref(c), B, d, h, d_h, _ptr(Wqkv), _ptr(pos), _ptr(head_idx),
                            head_idx.shape[-1], _ptr(head_count), _dt(Wqkv), _ptr(ws), ws.numel(),
                            _stream(stream)), "dv_kv_repair")
+
+
+# --------------------------------------------------------------------- labels
+
+def dv_label_workspace_size(T: int, d: int, N: int, h: int, d_h: int) -> int:
+    n = ctypes.c_size_t(0)
+    _ok(lib().dv_label_workspace_size(T, d, N, h, d_h, ctypes.byref(n)), "dv_label_workspace_size")
+    return n.value
+
+
+def dv_label_neurons(X, W1n, norms, ws, stream=None):
+    T, d = X.shape
+    _ok(lib().dv_label_neurons(_ptr(X), T, d, W1n.shape[0], _ptr(W1n), _dt(X), _ptr(norms), _ptr(ws),
+                               ws.numel(), _stream(stream)), "dv_label_neurons")
+
+
+def dv_label_heads(X, Wqkv, scale, norms, ws, stream=None):
+    T, d = X.shape
+    h, _, d_h, _ = Wqkv.shape
+    _ok(lib().dv_label_heads(_ptr(X), T, d, h, d_h, _ptr(Wqkv), float(scale), _dt(X), _ptr(norms), _ptr(ws),
+                             ws.numel(), _stream(stream)), "dv_label_heads")
+
+
+def dv_select_scores(scores, mode, k, t, idx, count, ws, stream=None):
+    B, N = scores.shape
+    _ok(lib().dv_select_scores(_ptr(scores), B, N, int(mode), int(k), float(t), _ptr(idx), idx.shape[-1],
+                               _ptr(count), _ptr(ws), ws.numel(), _stream(stream)), "dv_select_scores")
 
 
 # --------------------------------------------------------------------- helpers

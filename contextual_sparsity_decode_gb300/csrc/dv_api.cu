@@ -117,6 +117,27 @@ AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
   return w;
 }
 
+struct LabelWs {
+  float* partial;
+  float* Q;
+  uint16_t* K;
+  uint16_t* V;
+};
+// neurons: per-tile sums [ceil(T/256)][N]; heads: per-block sums
+// [h][ceil(T/32)] and Q (fp32), K, V (16-bit) [h][T][d_h]
+LabelWs carve_label(Carver& c, int T, int N, int h, int d_h, bool heads) {
+  LabelWs w{};
+  if (!heads) {
+    w.partial = c.take<float>((size_t)((T + 255) / 256) * N);
+  } else {
+    w.partial = c.take<float>((size_t)h * ((T + 31) / 32));
+    w.Q = c.take<float>((size_t)h * T * d_h);
+    w.K = c.take<uint16_t>((size_t)h * T * d_h);
+    w.V = c.take<uint16_t>((size_t)h * T * d_h);
+  }
+  return w;
+}
+
 // ---- validation ---------------------------------------------------------------------
 
 dv_status check_pred(const void* y, int B, int d, dv_dtype dt, const dv_predictor* preds,
@@ -365,6 +386,73 @@ dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h, const void
   AttnLaunch L = make_attn(nullptr, B, d, h, d_h, Wqkv, nullptr, kv, pos, head_idx, cap, head_count,
                            1.f, nullptr, 0, w);
   cudaError_t e = launch_kv_repair(L, dt, static_cast<WsHeader*>(ws), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+// ---- true-sparsity labels ----------------------------------------------------------------------
+
+dv_status dv_label_workspace_size(int T, int d, int N, int h, int d_h, size_t* bytes) {
+  if (!bytes || T < 1 || d < 1 || N < 0 || h < 0 || d_h < 0) return DV_ERR_INVALID_ARG;
+  Carver a(nullptr), b(nullptr);
+  carve_label(a, T, N, h, d_h, false);
+  carve_label(b, T, N, h, d_h, true);
+  *bytes = a.size() > b.size() ? a.size() : b.size();
+  return DV_OK;
+}
+
+namespace {
+dv_status check_label(const void* X, int T, int d, dv_dtype dt, const float* norms, void* ws) {
+  if (!dtype_ok(dt)) return DV_ERR_DTYPE;
+  if (dt == DV_F32) return DV_ERR_DTYPE;  // tensor-core products: 16-bit storage
+  if (!X || !norms || !ws || !aligned16(X) || !aligned4(norms) || !aligned16(ws)) return DV_ERR_INVALID_ARG;
+  if (T < 1 || T > (1 << 20) || d < 8 || d % 8 || d > 65536) return DV_ERR_INVALID_ARG;
+  return DV_OK;
+}
+}  // namespace
+
+dv_status dv_label_neurons(const void* X, int T, int d, int N, const void* W1n, dv_dtype dt, float* norms,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dv_status st = check_label(X, T, d, dt, norms, ws);
+  if (st != DV_OK) return st;
+  if (!W1n || !aligned16(W1n) || N < 1) return DV_ERR_INVALID_ARG;
+  Carver meas(nullptr);
+  carve_label(meas, T, N, 0, 0, false);
+  if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
+  Carver c(ws);
+  LabelWs w = carve_label(c, T, N, 0, 0, false);
+  LabelLaunch L{};
+  L.X = X; L.T = T; L.d = d; L.W1n = W1n; L.N = N; L.norms = norms; L.partial = w.partial;
+  cudaError_t e = launch_label_neurons(L, dt, static_cast<WsHeader*>(ws), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+dv_status dv_label_heads(const void* X, int T, int d, int h, int d_h, const void* Wqkv, float scale,
+                         dv_dtype dt, float* norms, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dv_status st = check_label(X, T, d, dt, norms, ws);
+  if (st != DV_OK) return st;
+  if (!Wqkv || !aligned16(Wqkv) || h < 1 || h > 1024) return DV_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return DV_ERR_UNSUPPORTED;
+  Carver meas(nullptr);
+  carve_label(meas, T, 0, h, d_h, true);
+  if (!ws_ok(ws, ws_bytes, meas.size())) return DV_ERR_WORKSPACE;
+  Carver c(ws);
+  LabelWs w = carve_label(c, T, 0, h, d_h, true);
+  LabelLaunch L{};
+  L.X = X; L.T = T; L.d = d; L.Wqkv = Wqkv; L.h = h; L.d_h = d_h; L.scale = scale; L.norms = norms;
+  L.partial = w.partial; L.Q = w.Q; L.K = w.K; L.V = w.V;
+  cudaError_t e = launch_label_heads(L, dt, static_cast<WsHeader*>(ws), stream);
+  return e == cudaSuccess ? DV_OK : cuda_fail(e);
+}
+
+dv_status dv_select_scores(const float* scores, int B, int N, dv_select mode, int k, float t, int32_t* idx, int cap,
+                    int32_t* count, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!scores || !idx || !count || !aligned4(scores) || !aligned4(idx) || !aligned4(count))
+    return DV_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || N < 1 || N > kSelectMaxN || cap < 1) return DV_ERR_INVALID_ARG;
+  if (mode != DV_TOPK && mode != DV_THRESHOLD) return DV_ERR_INVALID_ARG;
+  if (mode == DV_TOPK && (k < 0 || k > N || k > cap)) return DV_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, sizeof(WsHeader))) return DV_ERR_WORKSPACE;
+  cudaError_t e = launch_select(scores, B, N, (int)mode, k, t, idx, cap, count, static_cast<WsHeader*>(ws), stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);
 }
 

@@ -166,6 +166,25 @@ bool kv_tc_supported(int d, int d_h, dv_dtype dt);
 cudaError_t launch_kv_repair_tc(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
                                 cudaStream_t stream);
 
+// ---- true-sparsity labels (k_label.cu) ----------------------------------------
+
+struct LabelLaunch {
+  const void* X; int T, d;          // sequence [T][d], storage type
+  const void* W1n; int N;           // neurons: W1n [N][d]
+  const void* Wqkv; int h, d_h;     // heads: Wqkv [h][3][d_h][d]
+  float scale;
+  float* norms;                     // out: [N] or [h]
+  // scratch
+  float* partial;                   // per-tile sums of squares
+  float* Q; void* K; void* V;       // heads: [h][T][d_h]
+};
+cudaError_t launch_label_neurons(const LabelLaunch& a, dv_dtype dt, WsHeader* hdr, cudaStream_t stream);
+cudaError_t launch_label_heads(const LabelLaunch& a, dv_dtype dt, WsHeader* hdr, cudaStream_t stream);
+
+// Top-k / threshold selection of rows of non-negative scores (k_predict.cu).
+cudaError_t launch_select(const float* scores, int B, int N, int mode, int k, float t, int32_t* idx, int cap,
+                          int32_t* count, WsHeader* hdr, cudaStream_t stream);
+
 // ---- weighted sum of selected rows, column-sliced (k_rows.cu) -----------------
 
 struct CombineLaunch {

@@ -267,16 +267,19 @@ bool fused_fits(int grid, int num_sms) {
   return (long long)n_sm * num_sms >= grid;
 }
 
-// Batch-1 path choice: the streaming pass for long rows.  DV_MLP_STREAM=1 or
-// 0 in the environment forces it on or off (measurement).
-bool use_stream(int d, dv_dtype dt) {
+// Batch-1 path choice: the streaming pass when the selected rows amount to
+// at least 64 MB (measured on GB300: OPT-175B-shaped, 121 MB: 36.9 against
+// 48.2 us; OPT-30B-shaped at 50 %, 411 MB: 85.1 against 120.9 us; below
+// ~40 MB the one-launch kernel wins: OPT-13B-shaped, 21 MB: 15.0 against
+// 19.0 us).  DV_MLP_STREAM=1 or 0 in the environment forces it on or off.
+bool use_stream(int d, int cap, dv_dtype dt) {
   static const int forced = [] {
     const char* e = getenv("DV_MLP_STREAM");
     return e ? atoi(e) : -1;
   }();
   if (!mlp_stream_supported(d, dt)) return false;
   if (forced >= 0) return forced != 0;
-  return (size_t)d * (dt == DV_F32 ? 4 : 2) >= 16384;
+  return 2.0 * cap * d * (dt == DV_F32 ? 4 : 2) >= 64.0 * (1 << 20);
 }
 
 template <typename T>
@@ -299,7 +302,7 @@ cudaError_t mlp_t(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms, c
   c.member = nullptr; c.words = 0;  // the activations already carry the masks
   c.B = L.B; c.out = L.out; c.accumulate = L.accumulate; c.hdr = hdr;
   const int C = L.d / Elem<T>::kVec;
-  if (L.B == 1 && use_stream(L.d, dt)) {
+  if (L.B == 1 && use_stream(L.d, L.cap, dt)) {
     if (!L.accumulate) {  // the streaming pass adds into out
       cudaError_t e = cudaMemsetAsync(L.out, 0, (size_t)L.d * sizeof(float), stream);
       if (e != cudaSuccess) return e;

@@ -35,12 +35,10 @@ namespace {
 
 constexpr int kTM = 128;                 // tile rows (M)
 constexpr int kKB = 64;                  // K elements per stage (one 128-byte row)
-// Ring depths: a CTA keeps its whole ring in flight, and a 128-row tile
-// streams at most ~1/128 of the union per CTA, so the rings fill the shared
-// memory (up: 10 x 20 KB, down: 8 x 24 KB at 32 rows) to keep enough bytes
-// in flight per SM for HBM bandwidth.
-constexpr int kSU = 10;
-constexpr int kSD = 8;
+// Ring depths: about 100 KB of stages per CTA, so that two CTAs share an SM
+// (measured on GB300: rings of 200 KB, one CTA per SM, were 1.3-1.5x slower).
+constexpr int kSU = 5;
+constexpr int kSD = 4;
 constexpr int kKChunk = 1024;            // union neurons per down-projection CTA
 constexpr long long kUnwindNs = 2000000000LL;  // two seconds
 constexpr uint32_t kTmemCols = 32;

@@ -441,6 +441,21 @@ cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_pr
 
 }  // namespace
 
+cudaError_t launch_select(const float* scores, int B, int N, int mode, int k, float t, int32_t* idx, int cap,
+                          int32_t* count, WsHeader* hdr, cudaStream_t stream) {
+  static PerDevice attr;  // function attributes are per device
+  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [] {
+    return (int)cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kSelectMaxN * sizeof(uint32_t)));
+  });
+  if (ea != cudaSuccess) return ea;
+  SelArgs sa{};
+  sa.s[0] = scores; sa.N[0] = N; sa.mode[0] = mode; sa.k[0] = k; sa.cap[0] = cap; sa.t[0] = t;
+  sa.idx[0] = idx; sa.count[0] = count;
+  return launch_k(select_kernel, dim3(B, 1), dim3(kSelThreads), (size_t)N * sizeof(uint32_t), stream, true, 1, sa,
+                  hdr);
+}
+
 cudaError_t launch_predict(const void* y, int B, int d, dv_dtype dt, const PredLaunch& p,
                            int n_preds, WsHeader* hdr, cudaStream_t stream) {
   switch (dt) {

@@ -254,6 +254,46 @@ dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h,
                        const int32_t* head_count, dv_dtype dt,
                        void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------- true-sparsity labels */
+
+/* Workspace bytes for dv_label_neurons (sequence of T tokens, N neurons)
+ * and dv_label_heads (h heads of d_h); one workspace serves both. */
+dv_status dv_label_workspace_size(int T, int d, int N, int h, int d_h,
+                                  size_t* bytes);
+
+/* Neuron labels ([blog] §1 Contextual Sparsity: MLP neurons whose outputs
+ * over the input sequence have a large L2 norm, read neuron by neuron):
+ *     norms[j] = sqrt( sum_t ReLU(X[t] . W1n[j])^2 ),  j < N,
+ * for a sequence X [T][d] (e.g. a prompt's MLP inputs).  The product runs
+ * on the tensor cores: 16-bit storage only (DV_F32 -> DV_ERR_DTYPE);
+ * d a multiple of 8; fp32 accumulation; per-tile sums added in a fixed
+ * order.  norms [N] fp32, device. */
+dv_status dv_label_neurons(const void* X, int T, int d, int N, const void* W1n,
+                           dv_dtype dt, float* norms, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Head labels ([blog] §1: attention heads whose output matrix over the
+ * sequence has a large L2 norm, taken before the output projection):
+ *     norms[i] = || H_i ||_F,  H_i[t] = softmax(scale q_t K_i[0..t]^T) V_i[0..t]
+ * (causal: token t attends to tokens 0..t), q_t = X[t] W_i^Q in fp32 and
+ * K/V = X W_i^{K,V} rounded to the storage type as a KV cache holds them.
+ * 16-bit storage only; d_h in {64, 128}; norms [h] fp32, device. */
+dv_status dv_label_heads(const void* X, int T, int d, int h, int d_h,
+                         const void* Wqkv, float scale, dv_dtype dt,
+                         float* norms, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* Selection over rows of non-negative, finite fp32 scores [B][N] (e.g. the
+ * label norms; [blog] §2: a threshold on the norm gives the labels): top-k
+ * (ties to the lower index) or score > t, ascending, into idx [B][cap] with
+ * count [B]; the same selection as dv_predict's.  N <= 53248.  ws: at
+ * least 256 bytes, zero-filled once (its error word: a threshold list
+ * longer than cap is truncated and reported as DV_ERR_CAPACITY). */
+dv_status dv_select_scores(const float* scores, int B, int N, dv_select mode,
+                           int k, float t, int32_t* idx, int cap,
+                           int32_t* count, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
 /* ---------------------------------------------------- decoder-step helpers */
 
 /* y_b = LayerNorm(x_b) without affine terms (eps given), rounded to the

@@ -33,7 +33,11 @@ design notes of the repository):
   * K/V are stored in the storage type, rounded to nearest even; q, scores,
     H_i and outputs stay in float64 here;
   * the decoder stack is pre-LayerNorm without affine terms (eps 1e-5) with
-    residual adds; the attention input y is what the cache's X stores.
+    residual adds; the attention input y is what the cache's X stores;
+  * the true-sparsity labels ([blog] §1) are norms over a sequence: a
+    neuron's is the L2 norm of its ReLU activations over the tokens, a
+    head's the Frobenius norm of its causal output matrix H_i before W_i^O;
+    a label set is the top-k norms or the norms above a threshold.
 
 Every function takes float64 numpy arrays (widened from the storage type by
 the caller) and returns float64 results (int32 for index lists).
@@ -62,4 +66,8 @@ from .core import (  # noqa: F401
     decode_layer,
     lookahead,
     decode_stack,
+    neuron_norms,
+    head_outputs_causal,
+    head_norms,
+    label,
 )

@@ -317,3 +317,57 @@ def decode_stack(r: np.ndarray, layers: List[dict], caches: List[KVCache],
             pending = lookahead(y_a, layers[l + 1], k_heads, k_neurons)
             src = y_a
     return r, sets
+
+
+# --------------------------------------------------------------------------
+# true-sparsity labels  ([blog] §1 Contextual Sparsity: run the sequence
+# through the layer, keep the heads and MLP neurons whose outputs have the
+# largest L2 norm; [blog] §2: a threshold on that norm splits units into
+# positive and negative examples for the predictor)
+# --------------------------------------------------------------------------
+
+def neuron_norms(X: np.ndarray, W1n: np.ndarray) -> np.ndarray:
+    """For every neuron j, the L2 norm over the sequence's tokens (the rows
+    of X [T][d]) of its activation ReLU(x_t . W^1[:, j]): the MLP's T x 4d
+    activation matrix read neuron by neuron (one norm per column).
+    Returns [N]."""
+    A = np.maximum(0.0, np.atleast_2d(X) @ W1n.T)
+    return np.sqrt((A * A).sum(axis=0))
+
+
+def head_outputs_causal(X: np.ndarray, Wqkv: np.ndarray, c: float,
+                        dtype: str) -> np.ndarray:
+    """Every head's output matrix H_i [T][d_h] over the sequence X [T][d]:
+    token t attends to tokens 0..t (itself included), with its query
+    x_t W_i^Q in float64 and the keys / values x_j W_i^{K,V} rounded to the
+    storage type, as the KV cache holds them.  Returns [h][T][d_h]."""
+    X = np.atleast_2d(np.asarray(X, dtype=np.float64))
+    T = X.shape[0]
+    h, _, d_h, _ = Wqkv.shape
+    out = np.zeros((h, T, d_h))
+    for i in range(h):
+        Q = X @ Wqkv[i, 0].T
+        K = round_to(X @ Wqkv[i, 1].T, dtype)
+        V = round_to(X @ Wqkv[i, 2].T, dtype)
+        for t in range(T):
+            out[i, t] = head_output(Q[t], K[: t + 1], V[: t + 1], c)
+    return out
+
+
+def head_norms(X: np.ndarray, Wqkv: np.ndarray, c: float, dtype: str) -> np.ndarray:
+    """For every head i, the L2 (Frobenius) norm of its output matrix H_i
+    over the sequence, taken before the output projection W_i^O (the page's
+    example leaves the final linear layer out).  Returns [h]."""
+    H = head_outputs_causal(X, Wqkv, c, dtype)
+    return np.sqrt((H * H).sum(axis=(1, 2)))
+
+
+def label(norms: np.ndarray, mode: str, k: Optional[int] = None,
+          t: Optional[float] = None) -> np.ndarray:
+    """The units labelled important: the k largest norms (ties to the lower
+    index) or every norm above t; ascending."""
+    if mode == "topk":
+        return select_topk(np.asarray(norms), k)
+    if mode == "threshold":
+        return select_threshold(np.asarray(norms), t)
+    raise ValueError(mode)

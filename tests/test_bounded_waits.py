@@ -129,3 +129,30 @@ def test_tensor_core_pipeline_waits_time_out_and_unwind():
     ref = _ref(W1n, W2n, y, sets)
     for b in range(16):
         assert_rel_l2(f64(out)[b], ref[b], "f16", f"row {b} after the timed-out call")
+
+
+def test_streaming_mlp_recovers_after_a_short_wait_limit():
+    """The streaming batch-1 MLP pass (selected rows >= 64 MB) under a 1 ns
+    limit.  Its bulk copies usually land inside the hardware's own suspend
+    window of mbarrier.try_wait, so whether a wait gives up depends on
+    timing and either status is accepted; a CTA that gives up still waits
+    for the copies it issued.  The next calls, with the normal limit, match
+    the oracle."""
+    W1n, W2n, y, sets, W1d, W2d, yd, idx, cnt = _mlp_case("tmostrm", 1, 12288, 49152, 2458, "f16")
+    ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(1, 12288, 49152, 2458))
+    out = torch.zeros(1, 12288, device="cuda")
+    prev = dv.dv_set_wait_limit_ns(1)
+    statuses = []
+    try:
+        for _ in range(3):
+            dv.dv_sparse_mlp(yd, W1d, W2d, idx, cnt, out, ws)
+            statuses.append(dv.dv_check(ws)[0])
+    finally:
+        dv.dv_set_wait_limit_ns(prev)
+    assert set(statuses) <= {0, TIMEOUT}, statuses
+    ref = _ref(W1n, W2n, y, sets)[0]
+    for _ in range(2):
+        out.zero_()
+        dv.dv_sparse_mlp(yd, W1d, W2d, idx, cnt, out, ws)
+        assert dv.dv_check(ws) == (0, 0)
+        assert_rel_l2(f64(out)[0], ref, "f16", "after the short-limit calls")

@@ -645,3 +645,148 @@ def test_kv_prefill_matches_append():
     core.kv_prefill(b, Wqkv, 7)
     assert np.array_equal(a.valid, b.valid)
     assert np.allclose(a.K, b.K, rtol=1e-13, atol=1e-13) and np.allclose(a.V, b.V, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# true-sparsity labels (the blog page, §1 Contextual Sparsity and §2)
+# ---------------------------------------------------------------------------
+
+def _labels_golden():
+    with open(os.path.join(GOLDEN, "labels_two_tokens.json")) as f:
+        return json.load(f)
+
+
+def _golden_wqkv(g):
+    Wqkv = np.zeros((2, 3, 1, 2))
+    for i in range(2):
+        Wqkv[i, 0, 0] = g["Wq"][i][0]
+        Wqkv[i, 1, 0] = [0.0, g["Wk_second"]]
+        Wqkv[i, 2, 0] = g["Wv"][i][0]
+    return Wqkv
+
+
+def check_labels_golden():
+    g = _labels_golden()
+    n = core.neuron_norms(np.array(g["X_neurons"], float), np.array(g["W1n"], float))
+    assert n.shape == (3,) and np.allclose(n, g["neuron_norms"], rtol=0, atol=1e-14)
+    Wqkv = _golden_wqkv(g)
+    X = np.array(g["X_heads"], float)
+    H = core.head_outputs_causal(X, Wqkv, 1.0, "f64")
+    assert np.allclose(H, g["head_outputs"], rtol=0, atol=1e-14)
+    assert np.allclose(core.head_norms(X, Wqkv, 1.0, "f64"), g["head_norms"], rtol=0, atol=1e-14)
+    assert core.label(n, "topk", 1).tolist() == g["top1_neurons"]
+    assert core.label(n, "topk", 2).tolist() == g["top2_neurons"]
+    assert core.label(n, "threshold", t=1.0).tolist() == g["threshold1_neurons"]
+    assert core.label(core.head_norms(X, Wqkv, 1.0, "f64"), "topk", 1).tolist() == g["top1_heads"]
+
+
+def test_labels_golden():
+    check_labels_golden()
+
+
+def check_neuron_norms_special_cases():
+    rng = RNG(71)
+    d, N = 12, 9
+    W1n = rng.standard_normal((N, d))
+    # one token: the norm is the activation itself, ReLU of the pre-activation
+    x = rng.standard_normal(d)
+    n1 = core.neuron_norms(x[None], W1n)
+    assert n1.shape == (N,) and np.allclose(n1, np.maximum(0.0, W1n @ x), rtol=0, atol=1e-13)
+    # squared norms add over blocks of tokens
+    X1, X2 = rng.standard_normal((4, d)), rng.standard_normal((3, d))
+    n12 = core.neuron_norms(np.vstack([X1, X2]), W1n)
+    assert np.allclose(n12 ** 2, core.neuron_norms(X1, W1n) ** 2 + core.neuron_norms(X2, W1n) ** 2,
+                       rtol=1e-12, atol=1e-12)
+    # explicit loops
+    X = rng.standard_normal((5, d))
+    ref = np.zeros(N)
+    for j in range(N):
+        s = 0.0
+        for t in range(5):
+            u = sum(X[t, i] * W1n[j, i] for i in range(d))
+            s += max(0.0, u) ** 2
+        ref[j] = math.sqrt(s)
+    assert np.allclose(core.neuron_norms(X, W1n), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_neuron_norms_special_cases():
+    check_neuron_norms_special_cases()
+
+
+def check_head_outputs_causal():
+    rng = RNG(72)
+    h, d_h, d, T = 3, 4, 8, 6
+    Wqkv = rng.standard_normal((h, 3, d_h, d)) * 0.5
+    X = rng.standard_normal((T, d))
+    for dtype in ("f64", "bf16"):
+        H = core.head_outputs_causal(X, Wqkv, 0.7, dtype)
+        # textbook causal attention (torch float64, boolean causal mask)
+        for i in range(h):
+            Q = torch.tensor(X @ Wqkv[i, 0].T)
+            K = torch.tensor(core.round_to(X @ Wqkv[i, 1].T, dtype))
+            V = torch.tensor(core.round_to(X @ Wqkv[i, 2].T, dtype))
+            ref = F.scaled_dot_product_attention(Q[None], K[None], V[None], is_causal=True, scale=0.7)[0]
+            assert np.allclose(H[i], ref.numpy(), rtol=1e-12, atol=1e-12)
+        # a prefix of the sequence has the same outputs (causality)
+        Hp = core.head_outputs_causal(X[:3], Wqkv, 0.7, dtype)
+        assert np.array_equal(Hp, H[:, :3])
+    # one token: the head output is its own value row
+    H1 = core.head_outputs_causal(X[:1], Wqkv, 0.7, "f64")
+    for i in range(h):
+        assert np.allclose(H1[i, 0], Wqkv[i, 2] @ X[0], rtol=0, atol=1e-13)
+    # W^Q = 0: uniform weights, running means of the value rows
+    Wz = Wqkv.copy()
+    Wz[:, 0] = 0.0
+    Hz = core.head_outputs_causal(X, Wz, 0.7, "f64")
+    for i in range(h):
+        Vr = X @ Wz[i, 2].T
+        assert np.allclose(Hz[i], np.cumsum(Vr, axis=0) / np.arange(1, T + 1)[:, None], rtol=1e-12,
+                           atol=1e-12)
+    # the norms are the Frobenius norms of these matrices
+    n = core.head_norms(X, Wqkv, 0.7, "f64")
+    assert np.allclose(n, [np.linalg.norm(core.head_outputs_causal(X, Wqkv, 0.7, "f64")[i]) for i in range(h)],
+                       rtol=1e-13, atol=0)
+
+
+def test_head_outputs_causal():
+    check_head_outputs_causal()
+
+
+def _neuron_norms_no_relu(X, W1n):
+    A = np.atleast_2d(X) @ W1n.T
+    return np.sqrt((A * A).sum(axis=0))
+
+
+def _neuron_norms_per_token(X, W1n):
+    A = np.maximum(0.0, np.atleast_2d(X) @ W1n.T)
+    return np.sqrt((A * A).sum(axis=1))
+
+
+def _head_outputs_not_causal(X, Wqkv, c, dtype):
+    X = np.atleast_2d(np.asarray(X, dtype=np.float64))
+    T = X.shape[0]
+    h, _, d_h, _ = Wqkv.shape
+    out = np.zeros((h, T, d_h))
+    for i in range(h):
+        Q = X @ Wqkv[i, 0].T
+        K = core.round_to(X @ Wqkv[i, 1].T, dtype)
+        V = core.round_to(X @ Wqkv[i, 2].T, dtype)
+        for t in range(T):
+            out[i, t] = core.head_output(Q[t], K, V, c)
+    return out
+
+
+LABEL_MUTANTS = [
+    ("neuron_norms", _neuron_norms_no_relu, [check_labels_golden, check_neuron_norms_special_cases]),
+    ("neuron_norms", _neuron_norms_per_token, [check_labels_golden, check_neuron_norms_special_cases]),
+    ("head_outputs_causal", _head_outputs_not_causal, [check_labels_golden, check_head_outputs_causal]),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pins", LABEL_MUTANTS,
+                         ids=[f"{m[0]}:{m[1].__name__}" for m in LABEL_MUTANTS])
+def test_planted_label_mistake_is_caught(monkeypatch, name, mutant, pins):
+    monkeypatch.setattr(core, name, mutant)
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            pin()

@@ -36,6 +36,8 @@ CASES = [
     ("batch32_bf16_opt30b_tc",    32, 7168, 28672, "bf16", 1434),
     ("batch32_f16_ragged_tc",     32, 768,  3000,  "f16",  77),
     ("batch8_f32_cuda_cores",     8, 512,   2048,  "f32",  103),
+    ("stream_ragged_f16",         1, 8200,  8400,  "f16",  2100),   # >= 64 MB: streaming pass
+    ("stream_f32",                1, 4096,  16384, "f32",  2100),
     ("all_neurons_f16",           1, 256,   1024,  "f16",  1024),
     ("one_neuron_f16",            1, 256,   1024,  "f16",  1),
 ]
@@ -178,3 +180,25 @@ def test_batch1_calls_share_one_workspace():
         else:
             ref = oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), np.array(kept))
             assert_rel_l2(got, ref, "f16", f"call {step}")
+
+
+def test_streaming_pass_out_of_range_index_and_reuse():
+    """The streaming batch-1 pass (selected rows >= 64 MB): an index outside
+    [0, N) is skipped and reported; the same workspace then serves a clean
+    call, accumulating into a residual."""
+    d, N, k = 8192, 16384, 2100
+    W1n, W2n = _weights("strm", d, N, "f16")
+    y = draw((1, d), 1.0, 209, "strm/y", "f16")
+    S = _sets("strm", 1, N, k)[0].clone()
+    S[7] = N + 11
+    S = torch.sort(S).values
+    out, st, info = _run(y, W1n, W2n, [S], k)
+    assert st == 5 and info == N + 11
+    kept = S[S < N].numpy()
+    assert_rel_l2(out[0], oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), kept), "f16", "valid part")
+    base = draw((1, d), 1.0, 209, "strm/base", "f32")
+    S2 = _sets("strm2", 1, N, k)[0]
+    out2, st2, _ = _run(y, W1n, W2n, [S2], k, accumulate=True, base=base)
+    assert st2 == 0
+    assert_rel_l2(out2[0] - f64(base)[0], oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), S2.numpy()),
+                  "f16", "accumulate")

@@ -29,12 +29,18 @@ def test_cache_is_keyed_by_device_id(tmp_path):
 
 
 def test_every_cached_attribute_uses_the_per_device_table():
-    """No CUDA source keeps a process-wide 'attribute already set' flag."""
+    """No CUDA source keeps a device attribute, an occupancy answer or a
+    device property in a process-wide variable."""
     import re
+    device_calls = re.compile(r"cudaFuncSetAttribute|cudaOccupancy|cudaDeviceGetAttribute|cudaGetSymbolAddress")
     for name in sorted(os.listdir(CSRC)):
         if not name.endswith((".cu", ".cuh")):
             continue
         src = open(os.path.join(CSRC, name)).read()
-        for m in re.finditer(r"static\s+(?:const\s+)?(bool|int)\s+\w+", src):
-            line = src[: m.start()].count("\n") + 1
-            pytest.fail(f"{name}:{line}: process-wide cache '{m.group(0)}'")
+        for m in re.finditer(r"static\s+(?:const\s+)?(bool|int)\s+\w+[^;]*", src):
+            stmt_end = src.find(";", m.end())
+            window = src[m.start(): src.find("\n", stmt_end) + 1 if stmt_end >= 0 else len(src)]
+            following = "\n".join(src[m.end():].splitlines()[:6])
+            if device_calls.search(window) or device_calls.search(following):
+                line = src[: m.start()].count("\n") + 1
+                pytest.fail(f"{name}:{line}: process-wide cache '{m.group(0)[:60]}'")
