@@ -78,6 +78,7 @@ struct MlpWs {
   int32_t* U;
   int32_t* U_count;
   uint32_t* member;
+  uint32_t* bm;
   uint16_t* act_hi;
   uint16_t* act_lo;
   float* act;
@@ -89,6 +90,7 @@ MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   w.U = c.take<int32_t>((size_t)N);
   w.U_count = c.take<int32_t>(4);
   w.member = c.take<uint32_t>((size_t)B * ((N + 31) / 32));
+  if (B > 1) w.bm = c.take<uint32_t>((size_t)(N + 31) / 32);
   if (B == 1) w.ctr = c.take<int32_t>(8);
   if (B >= kTcMinBatch) {
     w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(N));
@@ -104,6 +106,12 @@ struct AttnWs {
   int32_t* slot_of;
   float* q;
   float* H;
+  int32_t* rows;
+  int32_t* rows_count;
+  uint32_t* need_bits;
+  uint8_t* miss;
+  uint16_t* act_hi;
+  uint16_t* act_lo;
 };
 AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
   AttnWs w{};
@@ -114,6 +122,14 @@ AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
   w.slot_of = c.take<int32_t>((size_t)h);
   w.q = c.take<float>((size_t)B * capU * d_h);
   w.H = c.take<float>((size_t)B * capU * d_h);
+  if (B >= kTcMinBatch) {  // tensor-core path (16-bit types)
+    w.rows = c.take<int32_t>((size_t)h * 3 * d_h);
+    w.rows_count = c.take<int32_t>(4);
+    w.need_bits = c.take<uint32_t>((size_t)(h + 31) / 32);
+    w.miss = c.take<uint8_t>((size_t)B * h);
+    w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(h * d_h));
+    w.act_lo = c.take<uint16_t>((size_t)32 * tc_act_cols(h * d_h));
+  }
   return w;
 }
 
@@ -197,6 +213,8 @@ AttnLaunch make_attn(const void* y, int B, int d, int h, int d_h, const void* Wq
   L.scale = scale; L.out = out; L.accumulate = accumulate ? 1 : 0;
   L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.slot_of = w.slot_of;
   L.q = w.q; L.H = w.H;
+  L.rows = w.rows; L.rows_count = w.rows_count; L.need_bits = w.need_bits; L.miss = w.miss;
+  L.act_hi = w.act_hi; L.act_lo = w.act_lo;
   return L;
 }
 }  // namespace
@@ -333,7 +351,7 @@ dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, con
   MlpLaunch L{};
   L.y = y; L.B = B; L.d = d; L.N = N; L.W1n = W1n; L.W2n = W2n;
   L.idx = idx; L.cap = cap; L.count = count; L.out = out; L.accumulate = accumulate ? 1 : 0;
-  L.U = w.U; L.U_count = w.U_count; L.member = w.member;
+  L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.bm = w.bm;
   L.act_hi = w.act_hi; L.act_lo = w.act_lo; L.act = w.act; L.ctr = w.ctr;
   cudaError_t e = launch_sparse_mlp(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);

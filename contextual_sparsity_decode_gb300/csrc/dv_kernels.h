@@ -103,6 +103,7 @@ struct MlpLaunch {
   float* out; int accumulate;
   // batch union scratch (B > 1)
   int32_t* U; int32_t* U_count; uint32_t* member;  // member [B][ceil(N/32)]
+  uint32_t* bm;                                     // [ceil(N/32)]: union bitmap of large batches
   // tensor-core path: activations split into two storage-type halves,
   // [32][tc_act_cols(N)] each
   void* act_hi; void* act_lo;
@@ -125,6 +126,30 @@ cudaError_t launch_sparse_mlp_tc(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
 cudaError_t launch_sparse_mlp(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
                               int num_sms, cudaStream_t stream);
 
+// Batched attention on the tensor cores (k_mlp_tc.cu; 8+ rows, 16-bit, d a
+// multiple of 128).  Projections of the union heads' Wqkv rows (`rows`,
+// `rows_count` on the device, at most max_rows) with the current tokens: q
+// of the member rows in fp32, K/V at pos rounded into the cache.
+struct TcQkvLaunch {
+  const void* y; int B, d, h, d_h, n_max, capQ;
+  const void* Wqkv;
+  const int32_t* rows; const int32_t* rows_count; int max_rows;
+  const uint32_t* member; int words;
+  const int32_t* slot_of; const int32_t* pos;
+  float* q; void* K; void* V;
+};
+cudaError_t launch_qkv_tc(const TcQkvLaunch& a, dv_dtype dt, WsHeader* hdr, cudaStream_t stream);
+// out[b] += sum_k coef[b][k] W[rows[k]] with the coefficients split into two
+// storage-type halves [32][Upad] (fp32 atomics into out).
+struct TcRowsLaunch {
+  const void* W; int n_rows, d, B;
+  int rows_per_unit;  // rows are listed in contiguous runs of this many (a head's d_h rows)
+  const int32_t* rows; const int32_t* rows_count; int max_rows;
+  void* act_hi; void* act_lo; int Upad;
+  float* out;
+};
+cudaError_t launch_rows_tc(const TcRowsLaunch& a, dv_dtype dt, WsHeader* hdr, cudaStream_t stream);
+
 // Batch 1, streaming pass over the selected rows with bulk copies into a
 // shared-memory ring (k_stream.cu); adds into out with atomics.
 bool mlp_stream_supported(int d, dv_dtype dt);
@@ -136,7 +161,8 @@ cudaError_t launch_mlp_stream(const void* y, int d, int N, const void* W1n, cons
 // (optional) slot_of[unit] = position of the unit in U.
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B,
                          int N, int32_t* U, int32_t* U_count, uint32_t* member,
-                         int32_t* slot_of, WsHeader* hdr, cudaStream_t stream);
+                         int32_t* slot_of, WsHeader* hdr, cudaStream_t stream,
+                         uint32_t* clear = nullptr, uint32_t* bm_global = nullptr);
 
 // ---- attention (k_attn.cu) ---------------------------------------------------
 
@@ -152,6 +178,10 @@ struct AttnLaunch {
   int32_t* U; int32_t* U_count; uint32_t* member; int32_t* slot_of;  // union (B > 1)
   float* q;                   // [B][capU][d_h]
   float* H;                   // [B][capU][d_h]
+  // batches on the tensor-core path (B >= kTcMinBatch), else null
+  int32_t* rows; int32_t* rows_count;   // expanded weight rows of the union heads
+  uint32_t* need_bits; uint8_t* miss;   // repair plan
+  void* act_hi; void* act_lo;           // [32][tc_act_cols(h * d_h)] output-projection coefficients
 };
 
 

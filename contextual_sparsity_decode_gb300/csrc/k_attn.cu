@@ -24,6 +24,8 @@
 // the missing positions: on the tensor cores for 16-bit storage
 // (k_kv_tc.cu), else the tiled CUDA-core GEMM below.
 
+#include <cstdlib>
+
 #include "dv_kernels.h"
 
 namespace dv {
@@ -55,6 +57,11 @@ struct AttnArgs {
   float* H;
   float* out;
   WsHeader* hdr;
+  // batches on the tensor-core path: attn_qkv only repairs, for the
+  // (row, head) pairs the planning kernel marked
+  int repair_only;
+  const uint32_t* need_bits;  // [ceil(h / 32)]: heads with a skipped position in some row
+  const uint8_t* miss;        // [B][h]: row b's selected head i has a skipped position
 };
 
 __device__ __forceinline__ bool member_of(const AttnArgs& a, int b, int i) {
@@ -380,9 +387,83 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   // The last CTA has the fewest tiles (tiles are dealt round-robin), so it
   // waits for y and appends before loading its first tile; nothing else is
   // live in its registers then.
-  if ((int)blockIdx.x == G - 1) {
+  if ((int)blockIdx.x == G - 1 && !a.repair_only) {  // repairs-only: the planning kernel appends
     grid_dep_wait();
     append();
+  }
+  if (a.repair_only) {
+    // The current tokens' projections run on the tensor cores; this kernel
+    // recomputes only the K/V rows of skipped positions, for the heads whose
+    // need bit the planning kernel set (U_s is reused for their list).
+    __syncthreads();  // every thread is done with U_s
+    if (tid < 32) {  // one warp compacts the bitmap (h <= 1024: 32 words)
+      const int lane = tid;
+      const uint32_t wv = lane < (a.h + 31) / 32 ? a.need_bits[lane] : 0u;
+      const int nb = __popc(wv);
+      int incl = nb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int off = incl - nb;
+      uint32_t mw = wv;
+      while (mw) {
+        U_s[off++] = lane * 32 + __ffs(mw) - 1;
+        mw &= mw - 1;
+      }
+      if (lane == 31) n_ent = incl;
+    }
+    __syncthreads();
+    const int n_need = n_ent;
+    const int rg_kv = 2 * a.d_h / rpc;  // K and V rows of a head
+    const int nt = n_need * rg_kv;
+    __syncthreads();  // n_ent is reused below
+    uint4 wr[kQR][kQC];
+    for (int t = blockIdx.x; t < nt; t += G) {
+      const int nh = t / rg_kv;
+      const int r0 = a.d_h + (t - nh * rg_kv) * rpc;
+      const int i = U_s[nh];
+      const int m = r0 / a.d_h, tbase = r0 - m * a.d_h;
+      const T* wbase = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
+      bool loaded = false;
+      for (int b = 0; b < a.B; ++b) {
+        const int p = row_pos(a, b);
+        if (p < 0 || !member_of(a, b, i) || !a.miss[(size_t)b * a.h + i]) continue;  // uniform
+        const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
+        for (int base = 0; base < p; base += kWin) {
+          const int j0 = base + tid * 16;
+          const uint4 v4 = j0 < p ? *reinterpret_cast<const uint4*>(vr + j0)
+                                  : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+          const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+          int mine = 0;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            mine += (j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0);
+          if (!__syncthreads_or(mine)) continue;
+          if (tid == 0) n_ent = 0;
+          __syncthreads();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int j = j0 + k;
+            if (j < p && ((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0) ent[atomicAdd(&n_ent, 1)] = (b << 20) | j;
+          }
+          __syncthreads();
+          if (one_pass && !loaded) {
+            qkv_load_w<T, kQC>(wbase, a.d, C, 0, tt, tpr, wr);
+            loaded = true;
+          }
+          uint4 ynone[kQC];
+          if (kPipe && one_pass)
+            qkv_entries_pipe<T, kQC, kStg>(a, ent, n_ent, wr, tl, m, tbase, i, 0, redb, xs_dyn, ynone, false,
+                                           []() {});
+          else
+            qkv_entries<T, kQC>(a, ent, n_ent, wr, one_pass, wbase, tl, m, tbase, i, 0, red, ynone, false, []() {});
+        }
+      }
+      __syncthreads();  // ent / n_ent are rebuilt for the next tile
+    }
+    return;
   }
   if ((int)blockIdx.x >= ntiles) return;  // uniform, before any barrier
   __syncthreads();
@@ -487,6 +568,89 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
     }
     __syncthreads();  // ent / n_ent are rebuilt for the next tile
   }
+}
+
+// ---------------------------------------------------------------------------
+// batches on the tensor-core path: planning, row lists, coefficient split
+
+// Which selected (row, head) pairs have a skipped position before the
+// current one: miss[b][i], and need_bits (zeroed by the union kernel) for
+// the heads with any such row.
+// CTA (0, b) also appends row b's token: X[b][pos] = y_b and the valid
+// column of pos (1 for the row's selected heads, else 0); the planning reads
+// positions before pos only.
+template <typename T>
+__global__ void __launch_bounds__(256) repair_plan_kernel(AttnArgs a, uint32_t* need_bits, uint8_t* miss) {
+  const int s = blockIdx.x, b = blockIdx.y;
+  const int cnt = max(0, min(a.head_count[b], a.cap));
+  if (s == 0) {
+    const int p = row_pos(a, b);
+    if (p < 0) {
+      if (threadIdx.x == 0) set_error(a.hdr, DV_ERR_POSITION, a.pos[b]);
+    } else {
+      const int C = a.d / Elem<T>::kVec;
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.y) + (size_t)b * a.d);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + ((size_t)b * a.n_max + p) * a.d);
+      for (int k = threadIdx.x; k < C; k += 256) dst[k] = ld_cached(src + k);
+      for (int i = threadIdx.x; i < a.h; i += 256) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 0;
+      __syncthreads();
+      for (int e = threadIdx.x; e < cnt; e += 256) {
+        const int i = a.head_idx[(size_t)b * a.cap + e];
+        if (i >= 0 && i < a.h) a.valid[((size_t)b * a.h + i) * a.n_max + p] = 1;
+      }
+    }
+  }
+  if (s >= cnt) return;
+  const int i = a.head_idx[(size_t)b * a.cap + s];
+  const int p = row_pos(a, b);
+  if (i < 0 || i >= a.h || p < 0) return;  // reported by the other kernels
+  const uint8_t* vr = a.valid + ((size_t)b * a.h + i) * a.n_max;
+  int any = 0;
+  for (int j0 = threadIdx.x * 16; j0 < p; j0 += 256 * 16) {
+    const uint4 v4 = *reinterpret_cast<const uint4*>(vr + j0);
+    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) any |= (j0 + k < p) && (((w4[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0);
+  }
+  any = __syncthreads_or(any);
+  if (threadIdx.x == 0) {
+    miss[(size_t)b * a.h + i] = any ? 1 : 0;
+    if (any) atomicOr(need_bits + (i >> 5), 1u << (i & 31));
+  }
+}
+
+// rows[k] = U[k / per] * per + k % per for the per rows of every union head
+// (per = 3 d_h: its Wqkv rows; per = d_h: its W^O rows), and their count.
+__global__ void expand_rows_kernel(const int32_t* U, const int32_t* U_count, int h, int per, int32_t* rows,
+                                   int32_t* rows_count) {
+  const int cnt = max(0, min(*U_count, h));
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k == 0) *rows_count = cnt * per;
+  if (k < cnt * per) {
+    const int u = k / per;
+    rows[k] = U[u] * per + (k - u * per);
+  }
+}
+
+// The output projection's coefficients for the tensor cores: H[b][u][t] of
+// the heads row b selected (0 elsewhere, and for the padding rows), split
+// into two storage-type halves hi + lo, laid out [BP][Upad].
+template <typename T>
+__global__ void coef_split_kernel(const float* H, int B, int capU, int d_h, const int32_t* U,
+                                  const int32_t* U_count, int h, const uint32_t* member, int words, T* hi, T* lo,
+                                  int Upad) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x, b = blockIdx.y;
+  if (k >= Upad) return;
+  const int cnt = max(0, min(*U_count, h));
+  float x = 0.f;
+  if (b < B && k < cnt * d_h) {
+    const int u = k / d_h;
+    const int i = U[u];
+    if (i >= 0 && i < h && bit_test(member + (size_t)b * words, i)) x = H[((size_t)b * capU + u) * d_h + (k - u * d_h)];
+  }
+  const T vh = Elem<T>::from_f(x);
+  hi[(size_t)b * Upad + k] = vh;
+  lo[(size_t)b * Upad + k] = Elem<T>::from_f(x - Elem<T>::to_f(vh));
 }
 
 // ---------------------------------------------------------------------------
@@ -842,6 +1006,9 @@ AttnArgs make_args(const AttnLaunch& L, WsHeader* hdr) {
   a.q = L.q; a.H = L.H;
   a.out = L.out; a.hdr = hdr;
   a.hwords = (L.h + 31) / 32;
+  a.repair_only = 0;
+  a.need_bits = L.need_bits;
+  a.miss = L.miss;
   if (L.B == 1) {
     a.U = L.head_idx; a.U_count = L.head_count; a.capU = L.cap;
     a.member = nullptr; a.slot_of = nullptr;
@@ -888,17 +1055,27 @@ bool decode_width_fits(int w) {
   }) == 1;
 }
 
+// With many (row, head) pairs the GPU is full anyway, and wider clusters
+// only add cluster barriers and co-scheduling constraints: from 64 pairs on
+// the cluster is 8 CTAs wide (each warp then takes several batches of
+// positions).  DV_DECODE_WIDTH in the environment forces a width (4..16).
 template <typename T, int DH>
-int decode_cluster_width(int n_max) {
+int decode_cluster_width(int n_max, int pairs) {
+  static const int forced = [] {
+    const char* e = getenv("DV_DECODE_WIDTH");
+    return e ? atoi(e) : 0;
+  }();
+  if (forced >= 4 && forced <= kMaxCSd && decode_width_fits<T, DH>(forced)) return forced;
   constexpr int kPos = kDecWarps * 16;  // positions per CTA in one batch (kPW = 16)
-  const int want = min(kMaxCSd, max(8, (n_max + kPos - 1) / kPos));
+  int want = min(kMaxCSd, max(8, (n_max + kPos - 1) / kPos));
+  if (pairs >= 64) want = 8;
   if (decode_width_fits<T, DH>(want)) return want;
   return decode_width_fits<T, DH>(8) ? 8 : 4;
 }
 
 template <typename T, int DH>
 cudaError_t launch_decode_dh(const AttnArgs& a, cudaStream_t stream) {
-  const int cw = decode_cluster_width<T, DH>(a.n_max);
+  const int cw = decode_cluster_width<T, DH>(a.n_max, a.B * a.cap);
   return launch_k(attn_decode_kernel<T, DH>, dim3(cw, a.cap, a.B), dim3(kDecThreads), 0, stream, true, cw, a);
 }
 
@@ -926,6 +1103,17 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   // three chunks per thread when a row fits (fewer registers), else four
   const int pdl = (launch_overlap() > 0 && a.B == 1) ? 1 : 0;
   cudaError_t e;
+  // batches of 8+ rows in a 16-bit type: the projections of the current
+  // tokens and the output projection are dense contractions over the union
+  // of the rows' heads and run on the tensor cores; attn_qkv only repairs
+  const bool tc = a.B > 1 && L.rows && tc_mlp_supported(a.B, a.d, dtype_of<T>());
+  if (tc) {
+    repair_plan_kernel<T><<<dim3(a.cap, a.B), 256, 0, stream>>>(a, L.need_bits, L.miss);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    a.repair_only = 1;
+  }
   // single-pass rows stage their vectors in dynamic shared memory
   const int C = a.d / Elem<T>::kVec;
   if (C <= (1 << tl) * 3) {
@@ -940,9 +1128,47 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
     e = launch_k(attn_qkv_kernel<T, 4>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
   }
   if (e != cudaSuccess) return e;
+  if (tc) {  // the current tokens' q and K/V
+    const int per = 3 * a.d_h;
+    expand_rows_kernel<<<(a.h * per + 255) / 256, 256, 0, stream>>>(a.U, a.U_count, a.h, per, L.rows, L.rows_count);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    TcQkvLaunch q{};
+    q.y = L.y; q.B = a.B; q.d = a.d; q.h = a.h; q.d_h = a.d_h; q.n_max = a.n_max; q.capQ = a.capU;
+    q.Wqkv = L.Wqkv; q.rows = L.rows; q.rows_count = L.rows_count;
+    q.max_rows = min(a.h, a.B * a.cap) * per;
+    q.member = a.member; q.words = a.hwords; q.slot_of = a.slot_of; q.pos = a.pos;
+    q.q = a.q; q.K = a.K; q.V = a.V;
+    e = launch_qkv_tc(q, dtype_of<T>(), hdr, stream);
+    if (e != cudaSuccess) return e;
+  }
   // 2. split-KV softmax, one cluster per (row, head), cache bookkeeping
   e = launch_decode<T>(a, stream);
   if (e != cudaSuccess) return e;
+  if (tc) {  // 3. output projection on the tensor cores
+    expand_rows_kernel<<<(a.h * a.d_h + 255) / 256, 256, 0, stream>>>(a.U, a.U_count, a.h, a.d_h, L.rows,
+                                                                      L.rows_count);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int Upad = tc_act_cols(a.h * a.d_h);
+    const int BP = a.B <= 16 ? 16 : 32;
+    coef_split_kernel<T><<<dim3((Upad + 255) / 256, BP), 256, 0, stream>>>(
+        a.H, a.B, a.capU, a.d_h, a.U, a.U_count, a.h, a.member, a.hwords, static_cast<T*>(L.act_hi),
+        static_cast<T*>(L.act_lo), Upad);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(2);
+    if (!L.accumulate) {  // the tensor-core combine adds into out
+      e = cudaMemsetAsync(L.out, 0, (size_t)a.B * a.d * sizeof(float), stream);
+      if (e != cudaSuccess) return e;
+    }
+    TcRowsLaunch r{};
+    r.W = L.Wo; r.n_rows = a.h * a.d_h; r.d = a.d; r.B = a.B; r.rows_per_unit = a.d_h;
+    r.rows = L.rows; r.rows_count = L.rows_count; r.max_rows = min(a.h, a.B * a.cap) * a.d_h;
+    r.act_hi = L.act_hi; r.act_lo = L.act_lo; r.Upad = Upad; r.out = L.out;
+    return launch_rows_tc(r, dtype_of<T>(), hdr, stream);
+  }
   // 3. output projection: out (+)= sum_u sum_t H[b][u][t] Wo[U[u]][t][:]
   CombineLaunch c{};
   c.W = L.Wo; c.d = a.d;
@@ -973,7 +1199,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch& L, dv_dtype dt, WsHeader* hdr, 
                                cudaStream_t stream) {
   if (L.B > 1) {
     cudaError_t e = launch_union(L.head_idx, L.cap, L.head_count, L.B, L.h, L.U, L.U_count,
-                                 L.member, L.slot_of, hdr, stream);
+                                 L.member, L.slot_of, hdr, stream, L.need_bits);
     if (e != cudaSuccess) return e;
   }
   switch (dt) {

@@ -199,32 +199,40 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // Union of the rows' lists: ascending U, |U|, and per-row membership bitmaps.
+// `clear` (optional, `words` long) is zeroed for a later kernel.
 __global__ void __launch_bounds__(1024) union_kernel(const int32_t* idx, int cap, const int32_t* count,
                                                      int B, int N, int32_t* U, int32_t* U_count,
                                                      uint32_t* member, int32_t* slot_of,
-                                                     WsHeader* hdr) {
+                                                     WsHeader* hdr, uint32_t* clear) {
   extern __shared__ uint32_t bm[];
   __shared__ int tmp[32];
   const int words = (N + 31) / 32;
   for (int i = threadIdx.x; i < words; i += blockDim.x) bm[i] = 0u;
   for (int i = threadIdx.x; i < B * words; i += blockDim.x) member[i] = 0u;
+  if (clear)
+    for (int i = threadIdx.x; i < words; i += blockDim.x) clear[i] = 0u;
   __syncthreads();
-  for (int b = 0; b < B; ++b) {
-    int cnt = count[b];
+  __shared__ int cnt_s[32];
+  if ((int)threadIdx.x < B) {  // every row's count in one round trip
+    int cnt = count[threadIdx.x];
     if (cnt > cap) {
-      if (threadIdx.x == 0) set_error(hdr, DV_ERR_CAPACITY, cnt);
+      set_error(hdr, DV_ERR_CAPACITY, cnt);
       cnt = cap;
     }
-    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-      const int j = idx[(size_t)b * cap + e];
-      if (j < 0 || j >= N) {
-        set_error(hdr, DV_ERR_INDEX_RANGE, j);
-        continue;
-      }
-      const uint32_t bit = 1u << (j & 31);
-      atomicOr(&bm[j >> 5], bit);
-      atomicOr(&member[(size_t)b * words + (j >> 5)], bit);
+    cnt_s[threadIdx.x] = max(cnt, 0);
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < B * cap; t += blockDim.x) {  // all rows' entries at once
+    const int b = t / cap, e = t - b * cap;
+    if (e >= cnt_s[b]) continue;
+    const int j = idx[(size_t)b * cap + e];
+    if (j < 0 || j >= N) {
+      set_error(hdr, DV_ERR_INDEX_RANGE, j);
+      continue;
     }
+    const uint32_t bit = 1u << (j & 31);
+    atomicOr(&bm[j >> 5], bit);
+    atomicOr(&member[(size_t)b * words + (j >> 5)], bit);
   }
   __syncthreads();
   const int WW = (words + 1023) / 1024;
@@ -247,6 +255,52 @@ __global__ void __launch_bounds__(1024) union_kernel(const int32_t* idx, int cap
 }
 
 
+// Large unions (many rows x long lists) in two passes: every entry marks
+// the union bitmap and its row's membership bitmap in global memory (both
+// zeroed before), spread over a grid; then one CTA lists the union.
+__global__ void __launch_bounds__(256) union_mark_kernel(const int32_t* idx, int cap, const int32_t* count, int N,
+                                                         uint32_t* bm, uint32_t* member, WsHeader* hdr) {
+  const int b = blockIdx.y, e = blockIdx.x * 256 + threadIdx.x;
+  const int words = (N + 31) / 32;
+  int cnt = count[b];
+  if (cnt > cap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(hdr, DV_ERR_CAPACITY, cnt);
+    cnt = cap;
+  }
+  if (e >= cnt) return;
+  const int j = idx[(size_t)b * cap + e];
+  if (j < 0 || j >= N) {
+    set_error(hdr, DV_ERR_INDEX_RANGE, j);
+    return;
+  }
+  const uint32_t bit = 1u << (j & 31);
+  atomicOr(bm + (j >> 5), bit);
+  atomicOr(member + (size_t)b * words + (j >> 5), bit);
+}
+
+__global__ void __launch_bounds__(1024) union_list_kernel(const uint32_t* bm, int N, int32_t* U, int32_t* U_count,
+                                                          int32_t* slot_of) {
+  __shared__ int tmp[32];
+  const int words = (N + 31) / 32;
+  const int WW = (words + 1023) / 1024;
+  const int w0 = min(words, (int)threadIdx.x * WW), w1 = min(words, w0 + WW);
+  int mine = 0;
+  for (int i = w0; i < w1; ++i) mine += __popc(bm[i]);
+  int total;
+  const int incl = block_inclusive_scan<1024>(mine, tmp, &total);
+  int o = incl - mine;
+  for (int i = w0; i < w1; ++i) {
+    uint32_t m = bm[i];
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      if (slot_of) slot_of[i * 32 + bit] = o;
+      U[o++] = i * 32 + bit;
+      m &= m - 1;
+    }
+  }
+  if (threadIdx.x == 0) *U_count = total;
+}
+
 template <typename T, int BT>
 cudaError_t launch_up(const UpArgs& a, int grid, cudaStream_t stream) {
   return launch_k(mlp_up_kernel<T, BT>, dim3(grid), dim3(kThreads), 0, stream, a.pdl != 0, 1, a);
@@ -268,10 +322,11 @@ bool fused_fits(int grid, int num_sms) {
 }
 
 // Batch-1 path choice: the streaming pass when the selected rows amount to
-// at least 64 MB (measured on GB300: OPT-175B-shaped, 121 MB: 36.9 against
-// 48.2 us; OPT-30B-shaped at 50 %, 411 MB: 85.1 against 120.9 us; below
-// ~40 MB the one-launch kernel wins: OPT-13B-shaped, 21 MB: 15.0 against
-// 19.0 us).  DV_MLP_STREAM=1 or 0 in the environment forces it on or off.
+// at least 96 MB (measured on GB300: OPT-175B-shaped, 121 MB: 36.9 against
+// 48.2 us; OPT-30B-shaped at 50 %, 411 MB: 85.1 against 120.9 us; at 41 MB
+// and below the one-launch kernel wins: OPT-13B-shaped, 21 MB: 15.0
+// against 19.0 us).  DV_MLP_STREAM=1 or 0 in the environment forces it on
+// or off.
 bool use_stream(int d, int cap, dv_dtype dt) {
   static const int forced = [] {
     const char* e = getenv("DV_MLP_STREAM");
@@ -279,7 +334,7 @@ bool use_stream(int d, int cap, dv_dtype dt) {
   }();
   if (!mlp_stream_supported(d, dt)) return false;
   if (forced >= 0) return forced != 0;
-  return 2.0 * cap * d * (dt == DV_F32 ? 4 : 2) >= 64.0 * (1 << 20);
+  return 2.0 * cap * d * (dt == DV_F32 ? 4 : 2) >= 96.0 * (1 << 20);
 }
 
 template <typename T>
@@ -348,9 +403,22 @@ int mlp_union_cap(int B, int N, int cap) {
 
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B, int N,
                          int32_t* U, int32_t* U_count, uint32_t* member, int32_t* slot_of,
-                         WsHeader* hdr, cudaStream_t stream) {
-  const size_t smem = (size_t)((N + 31) / 32) * sizeof(uint32_t);
-  union_kernel<<<1, 1024, smem, stream>>>(idx, cap, count, B, N, U, U_count, member, slot_of, hdr);
+                         WsHeader* hdr, cudaStream_t stream, uint32_t* clear, uint32_t* bm_global) {
+  const size_t words = (size_t)((N + 31) / 32);
+  if (bm_global && (long long)B * cap > 8192 && !clear) {  // two passes over a grid
+    cudaError_t e = cudaMemsetAsync(bm_global, 0, words * sizeof(uint32_t), stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(member, 0, (size_t)B * words * sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+    union_mark_kernel<<<dim3((cap + 255) / 256, B), 256, 0, stream>>>(idx, cap, count, N, bm_global, member, hdr);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    union_list_kernel<<<1, 1024, 0, stream>>>(bm_global, N, U, U_count, slot_of);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(2);
+    return e;
+  }
+  const size_t smem = words * sizeof(uint32_t);
+  union_kernel<<<1, 1024, smem, stream>>>(idx, cap, count, B, N, U, U_count, member, slot_of, hdr, clear);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(1);
   return e;
@@ -366,7 +434,7 @@ cudaError_t launch_sparse_mlp(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, in
   }
   if (L.B > 1) {
     e = launch_union(L.idx, L.cap, L.count, L.B, L.N, L.U, L.U_count, L.member, nullptr, hdr,
-                     stream);
+                     stream, nullptr, L.bm);
     if (e != cudaSuccess) return e;
   }
   if (tc) return launch_sparse_mlp_tc(L, dt, hdr, stream);

@@ -53,7 +53,22 @@ struct UpArgs {
   void* act_lo;
   WsHeader* hdr;
   long long wait_ns;
+  // 1: every 128-row tile of the row list is contiguous in the weight matrix
+  // (the attention's head blocks): one TMA tile load instead of 32 gathers
+  int tile_rows;
+  // kEpiQkv: row r of Wqkv [h * 3 * d_h][d] is (head r / (3 d_h), matrix, element)
+  int h, d_h, n_max, capQ;
+  const int32_t* slot_of;   // head -> slot in the batch union (q rows)
+  const int32_t* pos;       // [B]
+  float* q;                 // [B][capQ][d_h]
+  void* K;
+  void* V;
 };
+
+// Epilogues of the up kernel: the MLP's masked ReLU split into two storage
+// halves, or the attention projections (q in fp32; K/V of the current token
+// rounded into the cache) of the rows that selected each head.
+enum TcEpi { kEpiMlp = 0, kEpiQkv = 1 };
 
 struct DownArgs {
   const int32_t* U;
@@ -62,16 +77,17 @@ struct DownArgs {
   float* out;
   WsHeader* hdr;
   long long wait_ns;
+  int tile_rows;  // 1: every 64-row chunk of the row list is contiguous (two tile loads a stage)
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <typename T, int BP>
+template <typename T, int BP, int EPI = kEpiMlp>
 __global__ void __launch_bounds__(128, 1)
     mlp_tc_up_kernel(const __grid_constant__ CUtensorMap mapW1, const __grid_constant__ CUtensorMap mapY,
-                     UpArgs a) {
+                     const __grid_constant__ CUtensorMap mapT, UpArgs a) {
   constexpr uint32_t kABytes = kTM * 128, kBBytes = BP * 128;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kSU], empty[kSU], done;
@@ -126,10 +142,14 @@ __global__ void __launch_bounds__(128, 1)
       }
       tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
       uint8_t* dA = sA + s * kABytes;
+      if (a.tile_rows) {
+        tc::tma_load_2d(dA, &mapT, kb * kKB, rows[0], &full[s]);
+      } else {
 #pragma unroll 4
-      for (int g = 0; g < kTM / 4; ++g)
-        tc::tma_gather4(dA + g * 512, &mapW1, kb * kKB, rows[4 * g], rows[4 * g + 1], rows[4 * g + 2],
-                        rows[4 * g + 3], &full[s]);
+        for (int g = 0; g < kTM / 4; ++g)
+          tc::tma_gather4(dA + g * 512, &mapW1, kb * kKB, rows[4 * g], rows[4 * g + 1], rows[4 * g + 2],
+                          rows[4 * g + 3], &full[s]);
+      }
       tc::tma_load_2d(sB + s * kBBytes, &mapY, kb * kKB, 0, &full[s]);
       issued = kb + 1;
     }
@@ -170,16 +190,33 @@ __global__ void __launch_bounds__(128, 1)
   const int u = u0 + tid;
   const bool live = ok && !flag_err && u < cnt;
   const int row = rows[tid];
-  T* hi = static_cast<T*>(a.act_hi);
-  T* lo = static_cast<T*>(a.act_lo);
+  if (EPI == kEpiMlp) {
+    T* hi = static_cast<T*>(a.act_hi);
+    T* lo = static_cast<T*>(a.act_lo);
 #pragma unroll
-  for (int b = 0; b < BP; ++b) {
-    float x = fmaxf(v[b], 0.f);
-    if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
-    const T h = Elem<T>::from_f(x);
-    const T l = Elem<T>::from_f(x - Elem<T>::to_f(h));
-    hi[(size_t)b * a.Upad + u] = h;
-    lo[(size_t)b * a.Upad + u] = l;
+    for (int b = 0; b < BP; ++b) {
+      float x = fmaxf(v[b], 0.f);
+      if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
+      const T h = Elem<T>::from_f(x);
+      const T l = Elem<T>::from_f(x - Elem<T>::to_f(h));
+      hi[(size_t)b * a.Upad + u] = h;
+      lo[(size_t)b * a.Upad + u] = l;
+    }
+  } else if (live) {
+    const int dh3 = 3 * a.d_h;
+    const int i = row / dh3, rem = row - i * dh3, m = rem / a.d_h, t = rem - m * a.d_h;
+    const int slot = m == 0 ? a.slot_of[i] : 0;
+    T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      if (b >= a.B || !bit_test(a.member + (size_t)b * a.words, i)) continue;
+      if (m == 0) {
+        a.q[((size_t)b * a.capQ + slot) * a.d_h + t] = v[b];
+      } else {
+        const int p = a.pos[b];
+        if (p >= 0 && p < a.n_max) dst[(((size_t)b * a.h + i) * a.n_max + p) * a.d_h + t] = Elem<T>::from_f(v[b]);
+      }
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -195,7 +232,8 @@ __global__ void __launch_bounds__(128, 1)
 template <typename T, int BP>
 __global__ void __launch_bounds__(128, 1)
     mlp_tc_down_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapHi,
-                       const __grid_constant__ CUtensorMap mapLo, DownArgs a) {
+                       const __grid_constant__ CUtensorMap mapLo, const __grid_constant__ CUtensorMap mapT,
+                       DownArgs a) {
   constexpr uint32_t kABytes = kKB * 256, kBBytes = BP * 128;  // A: 64 neurons x 128 columns
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kSD], empty[kSD], done;
@@ -251,12 +289,17 @@ __global__ void __launch_bounds__(128, 1)
       tc::mbar_arrive_expect_tx(&full[s], kABytes + 2 * kBBytes);
       uint8_t* dA = sA + s * kABytes;
       const int* rr = rows + kb * kKB;
+      if (a.tile_rows) {
+        tc::tma_load_2d(dA, &mapT, c0, rr[0], &full[s]);
+        tc::tma_load_2d(dA + kKB * 128, &mapT, c0 + 64, rr[0], &full[s]);
+      } else {
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
+        for (int half = 0; half < 2; ++half)
 #pragma unroll 4
-        for (int g = 0; g < kKB / 4; ++g)
-          tc::tma_gather4(dA + half * (kKB * 128) + g * 512, &mapW2, c0 + half * 64, rr[4 * g], rr[4 * g + 1],
-                          rr[4 * g + 2], rr[4 * g + 3], &full[s]);
+          for (int g = 0; g < kKB / 4; ++g)
+            tc::tma_gather4(dA + half * (kKB * 128) + g * 512, &mapW2, c0 + half * 64, rr[4 * g], rr[4 * g + 1],
+                            rr[4 * g + 2], rr[4 * g + 3], &full[s]);
+      }
       tc::tma_load_2d(sH + s * kBBytes, &mapHi, k0 + kb * kKB, 0, &full[s]);
       tc::tma_load_2d(sL + s * kBBytes, &mapLo, k0 + kb * kKB, 0, &full[s]);
       issued = kb + 1;
@@ -371,18 +414,84 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   const int maxU = L.N < L.B * L.cap ? L.N : L.B * L.cap;
   UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr,
             wait_limit_ns()};
-  mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, 128, smem_up, stream>>>(mW1, mY, ua);
+  mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, 128, smem_up, stream>>>(mW1, mY, mW1, ua);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr, wait_limit_ns()};
   dim3 g(L.d / kTM, (maxU + kKChunk - 1) / kKChunk);
-  mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW2, mHi, mLo, da);
+  mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW2, mHi, mLo, mW2, da);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(2);
   return e;
 }
 
+template <typename T, int BP>
+cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream) {
+  constexpr bool bf16 = !std::is_same<T, __half>::value;
+  const int nrows = L.h * 3 * L.d_h;
+  CUtensorMap mW, mY, mT;
+  if (!make_map(&mW, L.Wqkv, L.d, nrows, 1, bf16) || !make_map(&mY, L.y, L.d, L.B, BP, bf16) ||
+      !make_map(&mT, L.Wqkv, L.d, nrows, kTM, bf16))
+    return cudaErrorInvalidValue;
+  const size_t smem_up = 1024 + kSU * (kTM * 128 + BP * 128);
+  static PerDevice attr;  // function attributes are per device
+  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [&] {
+    return (int)cudaFuncSetAttribute(mlp_tc_up_kernel<T, BP, kEpiQkv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_up);
+  });
+  if (ea != cudaSuccess) return ea;
+  UpArgs ua{};
+  ua.U = L.rows; ua.U_count = L.rows_count; ua.capU = nrows; ua.member = L.member; ua.words = L.words;
+  ua.B = L.B; ua.d = L.d; ua.N = nrows; ua.hdr = hdr; ua.wait_ns = wait_limit_ns();
+  ua.h = L.h; ua.d_h = L.d_h; ua.n_max = L.n_max; ua.capQ = L.capQ; ua.slot_of = L.slot_of; ua.pos = L.pos;
+  ua.q = L.q; ua.K = L.K; ua.V = L.V;
+  // a head's 3 d_h rows are contiguous: with d_h = 128 every 128-row tile is
+  // one head's Q, K or V block
+  ua.tile_rows = (3 * L.d_h) % kTM == 0 ? 1 : 0;
+  mlp_tc_up_kernel<T, BP, kEpiQkv><<<(L.max_rows + kTM - 1) / kTM, 128, smem_up, stream>>>(mW, mY, mT, ua);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
+}
+
+template <typename T, int BP>
+cudaError_t run_rows_tc(const TcRowsLaunch& L, WsHeader* hdr, cudaStream_t stream) {
+  constexpr bool bf16 = !std::is_same<T, __half>::value;
+  CUtensorMap mW, mHi, mLo, mT;
+  if (!make_map(&mW, L.W, L.d, L.n_rows, 1, bf16) || !make_map(&mHi, L.act_hi, L.Upad, BP, BP, bf16) ||
+      !make_map(&mLo, L.act_lo, L.Upad, BP, BP, bf16) || !make_map(&mT, L.W, L.d, L.n_rows, kKB, bf16))
+    return cudaErrorInvalidValue;
+  const size_t smem_dn = 1024 + kSD * (kKB * 256 + 2 * BP * 128);
+  static PerDevice attr;  // function attributes are per device
+  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [&] {
+    return (int)cudaFuncSetAttribute(mlp_tc_down_kernel<T, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_dn);
+  });
+  if (ea != cudaSuccess) return ea;
+  DownArgs da{L.rows, L.rows_count, L.n_rows, L.B, L.d, L.n_rows, L.out, hdr, wait_limit_ns(),
+              L.rows_per_unit % kKB == 0 ? 1 : 0};
+  dim3 g(L.d / kTM, (L.max_rows + kKChunk - 1) / kKChunk);
+  mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW, mHi, mLo, mT, da);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
+}
+
 }  // namespace
+
+cudaError_t launch_qkv_tc(const TcQkvLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
+  if (dt == DV_F16) return L.B <= 16 ? run_qkv_tc<__half, 16>(L, hdr, stream) : run_qkv_tc<__half, 32>(L, hdr, stream);
+  if (dt == DV_BF16)
+    return L.B <= 16 ? run_qkv_tc<__nv_bfloat16, 16>(L, hdr, stream) : run_qkv_tc<__nv_bfloat16, 32>(L, hdr, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rows_tc(const TcRowsLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
+  if (dt == DV_F16) return L.B <= 16 ? run_rows_tc<__half, 16>(L, hdr, stream) : run_rows_tc<__half, 32>(L, hdr, stream);
+  if (dt == DV_BF16)
+    return L.B <= 16 ? run_rows_tc<__nv_bfloat16, 16>(L, hdr, stream) : run_rows_tc<__nv_bfloat16, 32>(L, hdr, stream);
+  return cudaErrorInvalidValue;
+}
 
 bool tc_mlp_supported(int B, int d, dv_dtype dt) {
   return dt != DV_F32 && B >= kTcMinBatch && B <= 32 && d % kTM == 0;

@@ -8,19 +8,19 @@
 // neither depends on anything computed in this call, so both can be in
 // flight from the start: the only dependency inside a neuron is that its
 // W^2 row is scaled by the activation computed from its W^1 row.  Persistent
-// CTAs (two per SM) each take a contiguous share of the neuron list and
-// stream its rows in the order W1n[j0], W2n[j0], W1n[j1], ... into a ring
-// of shared-memory stages (one or more rows each) with bulk copies
-// (cp.async.bulk, issued by one thread, completing on an mbarrier).  All
-// threads take a stage as it lands: a W^1 row is dotted with y (y held in
-// registers, one 16-byte chunk slice per thread) and reduced across the CTA
-// into the neuron's activation ReLU(z); a W^2 row is scaled by it into the
-// thread's slice of a private output accumulator.  At the end every CTA
-// adds its accumulator to out with 16-byte vector atomics (so out must hold
-// 0 or the residual before the call, and the summation order across CTAs
-// is not fixed).  The path pays off for long lists of long rows, where each
-// CTA streams several hundred KB: a few dependent kernel steps would leave
-// the memory system idle for longer than the ring takes to fill.
+// CTAs (two per SM) each take a contiguous share of the neuron list.  One
+// elected thread streams the share's rows into a ring of shared-memory
+// stages with bulk copies (cp.async.bulk, completing on an mbarrier); all
+// threads take a stage as it lands: the row dots with y (y held in
+// registers, one 16-byte chunk slice per thread), one block reduction per
+// stage, ReLU, then the W^2 rows scaled into the thread's slice of a
+// private output accumulator.  At the end every CTA adds its accumulator to
+// out with 16-byte vector atomics (so out must hold 0 or the residual
+// before the call, and the summation order across CTAs is not fixed).  The
+// path pays off for long lists of long rows, where each CTA streams several
+// hundred KB; a stage is one or more whole neurons (measured on GB300:
+// stages of one row each, with a block barrier per row, were 1.1-1.4x
+// slower).
 //
 // Every wait is bounded (dv_set_wait_limit_ns) and reports DV_ERR_TIMEOUT;
 // a CTA that gives up still waits (at least two seconds) for the copies it
@@ -33,8 +33,8 @@ namespace dv {
 namespace {
 
 constexpr int kSThreads = 256;
-constexpr int kMaxSt = 10;      // ring stages
-constexpr int kMaxR = 8;        // rows per stage
+constexpr int kMaxSt = 6;       // ring stages
+constexpr int kMaxR = 8;        // neurons per stage
 constexpr int kMaxItems = 512;  // neurons per CTA
 constexpr long long kUnwindNs = 2000000000LL;
 constexpr int kMaxRing = 160 * 1024;  // shared-memory ring, at most
@@ -46,7 +46,7 @@ struct StreamMlpArgs {
   const int32_t* list;
   const int32_t* list_count;
   int cap, N, d;
-  int R, S;             // rows per stage, stages
+  int R, S;             // neurons per stage, stages
   uint32_t row_bytes;   // d * sizeof(T)
   float* out;
   WsHeader* hdr;
@@ -61,7 +61,6 @@ __global__ void __launch_bounds__(kSThreads) mlp_stream_kernel(StreamMlpArgs a) 
   __shared__ uint64_t full[kMaxSt];
   __shared__ float red[kSThreads / 32][kMaxR];
   __shared__ int nid_s[kMaxItems];
-  __shared__ float act_s[kMaxItems];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int C = a.d / V;
   const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
@@ -88,25 +87,24 @@ __global__ void __launch_bounds__(kSThreads) mlp_stream_kernel(StreamMlpArgs a) 
     tc::fence_mbar_init();
   }
   __syncthreads();
-  // units: 2 per neuron, W1n[j] then W2n[j]; a stage holds R units
-  const int nu_all = 2 * n;
-  const int nst = (nu_all + a.R - 1) / a.R;
-  const size_t stage_bytes = (size_t)a.R * a.row_bytes;
+  const int nst = (n + a.R - 1) / a.R;
+  const size_t stage_bytes = (size_t)a.R * 2 * a.row_bytes;
   const T* W1 = static_cast<const T*>(a.W1n);
   const T* W2 = static_cast<const T*>(a.W2n);
   int issued = 0;  // thread 0 only
   auto issue = [&](int q) {
     uint8_t* buf = ring + (size_t)(q % a.S) * stage_bytes;
-    const int u0 = q * a.R, u1 = min(nu_all, u0 + a.R);
+    const int i0 = q * a.R, i1 = min(n, i0 + a.R);
     uint32_t bytes = 0;
-    for (int u = u0; u < u1; ++u)
-      if (nid_s[u >> 1] >= 0) bytes += a.row_bytes;
+    for (int it = i0; it < i1; ++it)
+      if (nid_s[it] >= 0) bytes += 2 * a.row_bytes;
     tc::mbar_arrive_expect_tx(&full[q % a.S], bytes);
-    for (int u = u0; u < u1; ++u) {
-      const int j = nid_s[u >> 1];
+    for (int it = i0; it < i1; ++it) {
+      const int j = nid_s[it];
       if (j < 0) continue;
-      const T* src = ((u & 1) ? W2 : W1) + (size_t)j * a.d;
-      tc::bulk_g2s(buf + (size_t)(u - u0) * a.row_bytes, src, a.row_bytes, &full[q % a.S]);
+      uint8_t* dst = buf + (size_t)(it - i0) * 2 * a.row_bytes;
+      tc::bulk_g2s(dst, W1 + (size_t)j * a.d, a.row_bytes, &full[q % a.S]);
+      tc::bulk_g2s(dst + a.row_bytes, W2 + (size_t)j * a.d, a.row_bytes, &full[q % a.S]);
     }
     issued = q + 1;
   };
@@ -139,60 +137,47 @@ __global__ void __launch_bounds__(kSThreads) mlp_stream_kernel(StreamMlpArgs a) 
       break;
     }
     const uint8_t* buf = ring + (size_t)(q % a.S) * stage_bytes;
-    const int u0 = q * a.R, nu = min(a.R, nu_all - u0);
-    // W1 units of the stage: row dots with y
-    bool any_w1 = false;
+    const int nit = min(a.R, n - q * a.R);
+    float part[kMaxR];
 #pragma unroll
-    for (int us = 0; us < kMaxR; ++us) {
-      if (us >= nu) break;
-      if (((u0 + us) & 1) == 0) {
-        any_w1 = true;
-        float part = 0.f;
-        const uint4* w = reinterpret_cast<const uint4*>(buf + (size_t)us * a.row_bytes);
+    for (int it = 0; it < kMaxR; ++it) {
+      part[it] = 0.f;
+      if (it < nit) {
+        const uint4* w1 = reinterpret_cast<const uint4*>(buf + (size_t)it * 2 * a.row_bytes);
 #pragma unroll
         for (int k = 0; k < kCh; ++k) {
           const int c = tid + k * kSThreads;
           if (c < C) {
             float wf[V], xf[V];
-            unpack<T>(w[c], wf);
+            unpack<T>(w1[c], wf);
             unpack<T>(yr[k], xf);
 #pragma unroll
-            for (int v = 0; v < V; ++v) part = fmaf(wf[v], xf[v], part);
+            for (int v = 0; v < V; ++v) part[it] = fmaf(wf[v], xf[v], part[it]);
           }
         }
-        part = warp_sum(part);
-        if (lane == 0) red[wid][us] = part;
+        part[it] = warp_sum(part[it]);
       }
     }
-    if (any_w1) {  // uniform: depends on q only
-      __syncthreads();
+    if (lane == 0)
 #pragma unroll
-      for (int us = 0; us < kMaxR; ++us) {
-        if (us >= nu) break;
-        const int u = u0 + us;
-        if ((u & 1) == 0) {
-          float z = 0.f;
+      for (int it = 0; it < kMaxR; ++it)
+        if (it < nit) red[wid][it] = part[it];
+    __syncthreads();
 #pragma unroll
-          for (int w = 0; w < kSThreads / 32; ++w) z += red[w][us];
-          if (tid == 0) act_s[u >> 1] = nid_s[u >> 1] >= 0 ? fmaxf(z, 0.f) : 0.f;
-        }
-      }
-      __syncthreads();  // act_s of this stage's neurons is visible
-    }
-    // W2 units: the row scaled by its neuron's activation
+    for (int it = 0; it < kMaxR; ++it) {
+      if (it >= nit) break;
+      if (nid_s[q * a.R + it] < 0) continue;  // skipped (out of range): no rows were copied
+      float z = 0.f;
 #pragma unroll
-    for (int us = 0; us < kMaxR; ++us) {
-      if (us >= nu) break;
-      const int u = u0 + us;
-      if ((u & 1) == 0 || nid_s[u >> 1] < 0) continue;
-      const float act = act_s[u >> 1];
-      const uint4* w = reinterpret_cast<const uint4*>(buf + (size_t)us * a.row_bytes);
+      for (int w = 0; w < kSThreads / 32; ++w) z += red[w][it];
+      const float act = fmaxf(z, 0.f);
+      const uint4* w2 = reinterpret_cast<const uint4*>(buf + (size_t)it * 2 * a.row_bytes + a.row_bytes);
 #pragma unroll
       for (int k = 0; k < kCh; ++k) {
         const int c = tid + k * kSThreads;
         if (c < C) {
           float wf[V];
-          unpack<T>(w[c], wf);
+          unpack<T>(w2[c], wf);
 #pragma unroll
           for (int v = 0; v < V; ++v) acc[k][v] = fmaf(act, wf[v], acc[k][v]);
         }
@@ -233,10 +218,10 @@ cudaError_t stream_t(const StreamMlpArgs& a0, int num_sms, cudaStream_t stream) 
   constexpr int V = Elem<T>::kVec;
   const int C = a.d / V;
   a.row_bytes = (uint32_t)(a.d * sizeof(T));
-  // stages of at least ~16 KB (one row or more), ~110 KB of ring per CTA
-  a.R = max(1, min(kMaxR, (int)(16384 / a.row_bytes)));
-  const size_t stage = (size_t)a.R * a.row_bytes;
-  a.S = max(2, min(kMaxSt, (int)((110 * 1024) / stage)));
+  // stages of ~32 KB (at least one neuron: two rows), ~100 KB of ring per CTA
+  a.R = max(1, min(kMaxR, (int)(32768 / (2 * a.row_bytes))));
+  const size_t stage = (size_t)a.R * 2 * a.row_bytes;
+  a.S = max(2, min(kMaxSt, (int)((100 * 1024) / stage)));
   const size_t smem = stage * a.S;
   // two CTAs per SM, each with at most kMaxItems neurons
   const int grid = max(2 * num_sms, (a.cap + kMaxItems - 1) / kMaxItems);
@@ -254,9 +239,9 @@ cudaError_t stream_t(const StreamMlpArgs& a0, int num_sms, cudaStream_t stream) 
 bool mlp_stream_supported(int d, dv_dtype dt) {
   const int V = dt == DV_F32 ? 4 : 8;
   const size_t row = (size_t)d * (dt == DV_F32 ? 4 : 2);
-  // two stages of one row fit the ring; the thread slices cover a row in
-  // at most 8 chunks
-  return d / V <= 8 * kSThreads && 2 * row <= (size_t)kMaxRing;
+  // two stages of one neuron (two rows) fit the ring; the thread slices
+  // cover a row in at most 8 chunks
+  return d / V <= 8 * kSThreads && 2 * (2 * row) <= (size_t)kMaxRing;
 }
 
 cudaError_t launch_mlp_stream(const void* y, int d, int N, const void* W1n, const void* W2n,

@@ -132,7 +132,7 @@ def test_tensor_core_pipeline_waits_time_out_and_unwind():
 
 
 def test_streaming_mlp_recovers_after_a_short_wait_limit():
-    """The streaming batch-1 MLP pass (selected rows >= 64 MB) under a 1 ns
+    """The streaming batch-1 MLP pass (selected rows >= 96 MB) under a 1 ns
     limit.  Its bulk copies usually land inside the hardware's own suspend
     window of mbarrier.try_wait, so whether a wait gives up depends on
     timing and either status is accepted; a CTA that gives up still waits

@@ -20,7 +20,7 @@ import torch
 
 import oracle
 from contextual_sparsity_decode_gb300 import binding as dv
-from dvtest import TORCH, assert_rel_l2, f64, within_ulp_product
+from dvtest import TORCH, assert_rel_l2, f64, within_ulp, within_ulp_product
 from synth import draw
 
 pytestmark = pytest.mark.gpu
@@ -39,6 +39,11 @@ CASES = [
     ("random_sizes_f16", 2, 256,  8,  64,  "f16",  [9, 4],        48,   8,    "rnd", "isq",  None),
     ("random_sizes_b1",  1, 384,  12, 64,  "f16",  [21],          48,   12,   "rnd", "isq",  None),
     ("opt13b_b1_bf16",   1, 5120, 40, 128, "bf16", [300],         320,  2,    12,    "isq",  0.02),
+    # 8+ rows of a 16-bit type: projections and output projection on the tensor cores,
+    # repairs of skipped heads planned per (row, head)
+    ("batch16_f16_tc",   16, 512, 8,  64,  "f16",  [20 + b for b in range(16)], 64, 6, 3, "isq", None),
+    ("batch32_bf16_tc",  32, 256, 8,  128, "bf16", [9 + (7 * b) % 23 for b in range(32)], 48, 5, "rnd",
+     "one", None),
 ]
 
 
@@ -265,6 +270,7 @@ WIDE = [
     ("opt30b_b1_half_bf16",     1, 7168,  56, 128, "bf16", 2047, 2048, 28),
     ("opt175b_b1_f16",          1, 12288, 96, 128, "f16",  2047, 2048, 20),
     ("opt175b_b8_f16",          8, 12288, 96, 128, "f16",  2047, 2048, 20),
+    ("opt30b_b32_bf16",         32, 7168, 56, 128, "bf16", 2047, 2048, 3),
 ]
 
 
@@ -272,8 +278,17 @@ WIDE = [
 def test_sparse_attn_wide(case):
     """OPT-30B / OPT-175B widths with a 2047-position dense prompt and one
     decode step at position 2047 (KV length 2048), several rows per batch
-    with their own head sets.  The oracle's prompt cache is built only for
-    the heads each row selects."""
+    with their own head sets.
+
+    Checked per row and selected head: every stored K/V row (prompt and
+    current position) within one unit in the last place of the exact
+    float64 product of its X row; then the output against the oracle's
+    formula (head_output per head, summed through W_i^O, float64) evaluated
+    on those verified rows.  At these widths the softmax is peaked (logit
+    std ~3 over 2048 keys), so a one-ulp rounding difference of a bf16 key
+    at a heavily weighted position alone moves the output by ~1e-3; the
+    output bar is therefore applied given identical cache contents, as it
+    is given identical index lists."""
     name, B, d, h, d_h, dtype, n_prompt, n_max, k = case
     dev = "cuda"
     scale = 1.0 / math.sqrt(d_h)
@@ -299,8 +314,16 @@ def test_sparse_attn_wide(case):
     assert st == 0, (st, info)
     got, y64 = f64(out), f64(y)
     for b in range(B):
-        c = oracle.KVCache.empty(h, n_max, d_h, d, dtype)
-        c.X[:n_prompt] = f64(Xp[b])
-        oracle.kv_prefill(c, Wqkv64, n_prompt, heads=sets[b].tolist())
-        ref = oracle.sparse_attn(y64[b], Wqkv64, Wo64, c, n_prompt, sets[b].tolist(), scale)
+        Xe = np.vstack([f64(Xp[b]), y64[b][None]])  # positions 0..n_prompt
+        ref = np.zeros(d)
+        for i in sets[b].tolist():
+            Kr = f64(kv.K[b, i, : n_prompt + 1])
+            Vr = f64(kv.V[b, i, : n_prompt + 1])
+            for got_r, m, what in ((Kr, 1, "K"), (Vr, 2, "V")):
+                exact = Xe @ Wqkv64[i, m].T
+                # fp32 accumulation of d products: ~sqrt(d) roundings of the running sum
+                acc = 4.0 * np.sqrt(d) * 2.0 ** -24 * np.abs(exact).max()
+                assert within_ulp(got_r, exact, dtype, acc_floor=acc), f"{name} row {b} head {i} {what}"
+            q = Wqkv64[i, 0] @ y64[b]
+            ref += oracle.head_output(q, Kr, Vr, scale) @ Wo64[i]
         assert_rel_l2(got[b], ref, dtype, f"{name} row {b}")

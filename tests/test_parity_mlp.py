@@ -36,8 +36,8 @@ CASES = [
     ("batch32_bf16_opt30b_tc",    32, 7168, 28672, "bf16", 1434),
     ("batch32_f16_ragged_tc",     32, 768,  3000,  "f16",  77),
     ("batch8_f32_cuda_cores",     8, 512,   2048,  "f32",  103),
-    ("stream_ragged_f16",         1, 8200,  8400,  "f16",  2100),   # >= 64 MB: streaming pass
-    ("stream_f32",                1, 4096,  16384, "f32",  2100),
+    ("stream_ragged_f16",         1, 8200,  8400,  "f16",  3100),   # >= 96 MB: streaming pass
+    ("stream_f32",                1, 4096,  16384, "f32",  3100),
     ("all_neurons_f16",           1, 256,   1024,  "f16",  1024),
     ("one_neuron_f16",            1, 256,   1024,  "f16",  1),
 ]
@@ -183,10 +183,10 @@ def test_batch1_calls_share_one_workspace():
 
 
 def test_streaming_pass_out_of_range_index_and_reuse():
-    """The streaming batch-1 pass (selected rows >= 64 MB): an index outside
+    """The streaming batch-1 pass (selected rows >= 96 MB): an index outside
     [0, N) is skipped and reported; the same workspace then serves a clean
     call, accumulating into a residual."""
-    d, N, k = 8192, 16384, 2100
+    d, N, k = 8192, 16384, 3100
     W1n, W2n = _weights("strm", d, N, "f16")
     y = draw((1, d), 1.0, 209, "strm/y", "f16")
     S = _sets("strm", 1, N, k)[0].clone()
@@ -202,3 +202,21 @@ def test_streaming_pass_out_of_range_index_and_reuse():
     assert st2 == 0
     assert_rel_l2(out2[0] - f64(base)[0], oracle.sparse_mlp(f64(y)[0], f64(W1n), f64(W2n), S2.numpy()),
                   "f16", "accumulate")
+
+
+def test_large_batch_union_with_out_of_range_index():
+    """16 rows x 600 neurons: the union is built in two passes over a grid;
+    an index outside [0, N) in one row is skipped and reported, every row
+    still matches its own set."""
+    B, d, N, k = 16, 1024, 4096, 600
+    W1n, W2n = _weights("bigu", d, N, "f16")
+    y = draw((B, d), 1.0, 210, "bigu/y", "f16")
+    sets = _sets("bigu", B, N, k)
+    bad = sets[5].clone()
+    bad[-1] = N + 2
+    sets[5] = bad
+    out, st, info = _run(y, W1n, W2n, sets, k)
+    assert st == 5 and info == N + 2
+    ref = oracle.sparse_mlp_batched(f64(y), f64(W1n), f64(W2n), [s[s < N].numpy() for s in sets])
+    for b in range(B):
+        assert_rel_l2(out[b], ref[b], "f16", f"row {b}")

@@ -158,6 +158,14 @@ def test_batched_stack_teacher_forced():
     _teacher_forced(w, B=3, steps=4)
 
 
+def test_batch8_stack_teacher_forced():
+    """Eight sequences: both sparse blocks take the tensor-core path (the
+    batch union as a dense contraction), accumulating into the residual."""
+    w = Workload("batch8_stack", 34, d=512, h=8, d_h=64, N=2048, r=128, dtype="f16", layers=2,
+                 n_prompt=24, n_gen=4, head_pct=25, neuron_pct=5)
+    _teacher_forced(w, B=8, steps=4)
+
+
 def test_opt13b_stack_all_layers_teacher_forced():
     """All 40 layers of the OPT-13B-shaped stack (d = 5120, 40 heads of 128,
     FFN 20480, rank-1024 predictors, 8 heads / 1024 neurons) after the
