@@ -83,8 +83,8 @@ __device__ __forceinline__ int row_pos(const AttnArgs& a, int b) {
 // current token of every batch row that selected the head, and (K/V rows)
 // the stored embedding X[j] of every position j < pos whose K/V were skipped.
 
-constexpr int kQCMax = 4;   // chunks per thread per pass over a row (3 or 4)
-constexpr int kQR = 4;      // rows per thread group (divides d_h)
+constexpr int kQCMax = 4;   // chunks per thread per pass over a row that fits 1024 chunks
+constexpr int kQR = 4;      // rows per thread group (divides d_h) with 3 chunks; else 2
 constexpr int kNE = 2;      // vectors per group of entries
 constexpr int kWin = 4096;  // positions scanned per repair window (256 x 16)
 
@@ -94,12 +94,12 @@ int qkv_tpr_log2(int chunks) {
   return l;
 }
 
-template <typename T, int kQC>
+template <typename T, int kQC, int QR>
 __device__ __forceinline__ void qkv_load_w(const T* wbase, int d, int C, int cb, int tt, int tpr,
-                                           uint4 (&w)[kQR][kQC]) {
+                                           uint4 (&w)[QR][kQC]) {
   constexpr int V = Elem<T>::kVec;
 #pragma unroll
-  for (int k = 0; k < kQR; ++k)
+  for (int k = 0; k < QR; ++k)
 #pragma unroll
     for (int j = 0; j < kQC; ++j) {
       const int c = cb + tt + j * tpr;
@@ -112,10 +112,10 @@ __device__ __forceinline__ void qkv_load_w(const T* wbase, int d, int C, int cb,
 // multiply-adds of the last group, `after_last_fma()` runs (all threads) while
 // the partial sums wait in registers: the persistent kernel uses it to issue
 // the next tile's weight loads into `w`.
-template <typename T, int kQC, typename F>
-__device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)[kQR][kQC],
+template <typename T, int kQC, int QR, typename F>
+__device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)[QR][kQC],
                             bool one_pass, const T* wbase, int tl, int m, int tbase, int i, int u,
-                            float (&red)[8][kQR][kNE], const uint4 (&ycur)[kQC], bool ycur_ok,
+                            float (&red)[8][QR][kNE], const uint4 (&ycur)[kQC], bool ycur_ok,
                             F&& after_last_fma) {
   constexpr int V = Elem<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -125,13 +125,13 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
   const T* X = static_cast<const T*>(a.X);
   for (int g0 = 0; g0 < n; g0 += kNE) {
     const int ne = min(kNE, n - g0);
-    float acc[kQR][kNE];
+    float acc[QR][kNE];
 #pragma unroll
-    for (int k = 0; k < kQR; ++k)
+    for (int k = 0; k < QR; ++k)
 #pragma unroll
       for (int e = 0; e < kNE; ++e) acc[k][e] = 0.f;
     for (int cb = 0; cb < C; cb += tpr * kQC) {
-      if (!one_pass) qkv_load_w<T, kQC>(wbase, a.d, C, cb, tt, tpr, w);
+      if (!one_pass) qkv_load_w<T, kQC, QR>(wbase, a.d, C, cb, tt, tpr, w);
 #pragma unroll
       for (int j = 0; j < kQC; ++j) {
         const int c = cb + tt + j * tpr;
@@ -146,7 +146,7 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
           if ((en & kCur) && ycur_ok) unpack<T>(ycur[j], xf);  // preloaded (batch 1, one pass)
           else unpack<T>(ld_cached(vec + (size_t)c * V), xf);
 #pragma unroll
-          for (int k = 0; k < kQR; ++k) {
+          for (int k = 0; k < QR; ++k) {
             float wf[V];
             unpack<T>(w[k][j], wf);
 #pragma unroll
@@ -157,7 +157,7 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
     }
     if (g0 + kNE >= n) after_last_fma();
 #pragma unroll
-    for (int k = 0; k < kQR; ++k)
+    for (int k = 0; k < QR; ++k)
 #pragma unroll
       for (int e = 0; e < kNE; ++e) {
         if (e >= ne) break;
@@ -166,13 +166,13 @@ __device__ void qkv_entries(const AttnArgs& a, const int* ent, int n, uint4 (&w)
       }
     __syncthreads();
     const int nw = tpr >> 5;
-    for (int q = tid; q < RS * kQR * ne; q += 256) {
-      const int sl = q / (kQR * ne), k = (q / ne) % kQR, e = q % ne;
+    for (int q = tid; q < RS * QR * ne; q += 256) {
+      const int sl = q / (QR * ne), k = (q / ne) % QR, e = q % ne;
       float z = 0.f;
       for (int x = 0; x < nw; ++x) z += red[sl * nw + x][k][e];
       const int en = ent[g0 + e];
       const int b = (en >> 20) & 1023, jp = en & 0xfffff;
-      const int t = tbase + sl * kQR + k;
+      const int t = tbase + sl * QR + k;
       if (m == 0) {
         a.q[((size_t)b * a.capU + u) * a.d_h + t] = z;
       } else {
@@ -205,9 +205,9 @@ __device__ __forceinline__ void cp_async_wait_stages() {
   cp_async_wait<S - 1>();
 }
 
-template <typename T, int kQC, int kStages, typename F>
-__device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4 (&w)[kQR][kQC], int tl,
-                                 int m, int tbase, int i, int u, float (&redb)[8][kGB][kQR][kNE],
+template <typename T, int kQC, int QR, int kStages, typename F>
+__device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4 (&w)[QR][kQC], int tl,
+                                 int m, int tbase, int i, int u, float (&redb)[8][kGB][QR][kNE],
                                  uint4* xs, const uint4 (&ycur)[kQC], bool ycur_ok, F&& after_last_fma) {
   constexpr int V = Elem<T>::kVec;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -248,9 +248,9 @@ __device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4
       issue(g + kStages - 1);
       cp_async_wait_stages<kStages>();  // group g has landed (for this thread)
       const int st = g % kStages;
-      float acc[kQR][kNE];
+      float acc[QR][kNE];
 #pragma unroll
-      for (int k = 0; k < kQR; ++k)
+      for (int k = 0; k < QR; ++k)
 #pragma unroll
         for (int e = 0; e < kNE; ++e) acc[k][e] = 0.f;
 #pragma unroll
@@ -265,7 +265,7 @@ __device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4
           if ((ent[idx] & kCur) && ycur_ok) unpack<T>(ycur[j], xf);
           else unpack<T>(*slot(st, e, j), xf);
 #pragma unroll
-          for (int k = 0; k < kQR; ++k) {
+          for (int k = 0; k < QR; ++k) {
             float wf[V];
             unpack<T>(w[k][j], wf);
 #pragma unroll
@@ -275,7 +275,7 @@ __device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4
       }
       if (g == ng - 1) after_last_fma();
 #pragma unroll
-      for (int k = 0; k < kQR; ++k)
+      for (int k = 0; k < QR; ++k)
 #pragma unroll
         for (int e = 0; e < kNE; ++e) {
           const float z = warp_sum(acc[k][e]);
@@ -284,17 +284,17 @@ __device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4
     }
     __syncthreads();
     const int nw = tpr >> 5;
-    const int per_g = RS * kQR * kNE;
+    const int per_g = RS * QR * kNE;
     for (int o = tid; o < per_g * gbn; o += 256) {
       const int q = o / per_g, r = o - q * per_g;
-      const int sl = r / (kQR * kNE), k = (r / kNE) % kQR, e = r % kNE;
+      const int sl = r / (QR * kNE), k = (r / kNE) % QR, e = r % kNE;
       const int idx = (gb0 + q) * kNE + e;
       if (idx >= n) continue;
       float z = 0.f;
       for (int x = 0; x < nw; ++x) z += redb[sl * nw + x][q][k][e];
       const int en = ent[idx];
       const int b = (en >> 20) & 1023, jp = en & 0xfffff;
-      const int t = tbase + sl * kQR + k;
+      const int t = tbase + sl * QR + k;
       if (m == 0) {
         a.q[((size_t)b * a.capU + u) * a.d_h + t] = z;
       } else {
@@ -312,20 +312,20 @@ __device__ void qkv_entries_pipe(const AttnArgs& a, const int* ent, int n, uint4
 // one selected head's W^Q, W^K or W^V block).  The next tile's weights (and,
 // batch 1, its valid flags) are requested right after the current tile's
 // multiply-adds, so they are in flight during its reduction and stores.
-template <typename T, int kQC>
+template <typename T, int kQC, int QR>
 __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, int tl, int pdl) {
   constexpr int V = Elem<T>::kVec;
   __shared__ int ent[kWin];
   __shared__ int n_ent;
-  __shared__ float red[8][kQR][kNE];
-  __shared__ float redb[8][kGB][kQR][kNE];
+  __shared__ float red[8][QR][kNE];
+  __shared__ float redb[8][kGB][QR][kNE];
   __shared__ int U_s[1024];
   extern __shared__ uint4 xs_dyn[];  // single-pass rows: staged vector chunks (qkv_entries_pipe)
   constexpr int kStg = qkv_stages(kQC);
   constexpr bool kPipe = kQC == 3;   // with 4 chunks the staging loop would spill
   const int tid = threadIdx.x;
   const int tpr = 1 << tl, RS = 256 >> tl, slot = tid >> tl, tt = tid & (tpr - 1);
-  const int rpc = RS * kQR;
+  const int rpc = RS * QR;
   const int G = (int)gridDim.x;
   const int C = a.d / V;
   const bool one_pass = C <= tpr * kQC;
@@ -419,13 +419,13 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
     const int rg_kv = 2 * a.d_h / rpc;  // K and V rows of a head
     const int nt = n_need * rg_kv;
     __syncthreads();  // n_ent is reused below
-    uint4 wr[kQR][kQC];
+    uint4 wr[QR][kQC];
     for (int t = blockIdx.x; t < nt; t += G) {
       const int nh = t / rg_kv;
       const int r0 = a.d_h + (t - nh * rg_kv) * rpc;
       const int i = U_s[nh];
       const int m = r0 / a.d_h, tbase = r0 - m * a.d_h;
-      const T* wbase = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
+      const T* wbase = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * QR) * a.d;
       bool loaded = false;
       for (int b = 0; b < a.B; ++b) {
         const int p = row_pos(a, b);
@@ -450,15 +450,15 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
           }
           __syncthreads();
           if (one_pass && !loaded) {
-            qkv_load_w<T, kQC>(wbase, a.d, C, 0, tt, tpr, wr);
+            qkv_load_w<T, kQC, QR>(wbase, a.d, C, 0, tt, tpr, wr);
             loaded = true;
           }
           uint4 ynone[kQC];
           if (kPipe && one_pass)
-            qkv_entries_pipe<T, kQC, kStg>(a, ent, n_ent, wr, tl, m, tbase, i, 0, redb, xs_dyn, ynone, false,
+            qkv_entries_pipe<T, kQC, QR, kStg>(a, ent, n_ent, wr, tl, m, tbase, i, 0, redb, xs_dyn, ynone, false,
                                            []() {});
           else
-            qkv_entries<T, kQC>(a, ent, n_ent, wr, one_pass, wbase, tl, m, tbase, i, 0, red, ynone, false, []() {});
+            qkv_entries<T, kQC, QR>(a, ent, n_ent, wr, one_pass, wbase, tl, m, tbase, i, 0, red, ynone, false, []() {});
         }
       }
       __syncthreads();  // ent / n_ent are rebuilt for the next tile
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
   if ((int)blockIdx.x >= ntiles) return;  // uniform, before any barrier
   __syncthreads();
 
-  uint4 w[kQR][kQC];
+  uint4 w[QR][kQC];
   uint4 vflags = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
   auto meta = [&](int t, int& i, int& m, int& tbase, int& u) {
     u = t / RG;
@@ -481,8 +481,8 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
     int i, m, tbase, u;
     meta(t, i, m, tbase, u);
     if (i < 0 || i >= a.h) return;
-    const T* wb = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
-    if (one_pass) qkv_load_w<T, kQC>(wb, a.d, C, 0, tt, tpr, w);
+    const T* wb = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * QR) * a.d;
+    if (one_pass) qkv_load_w<T, kQC, QR>(wb, a.d, C, 0, tt, tpr, w);
     vflags = make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
     if (a.B == 1 && m > 0 && p0 >= 0 && p0 <= kWin && tid * 16 < p0)
       vflags = *reinterpret_cast<const uint4*>(a.valid + (size_t)i * a.n_max + tid * 16);
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
       if (tn < ntiles) fetch(tn);
       continue;
     }
-    const T* wbase = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * kQR) * a.d;
+    const T* wbase = static_cast<const T*>(a.Wqkv) + ((size_t)(i * 3 + m) * a.d_h + tbase + slot * QR) * a.d;
     const bool fast_scan = a.B == 1 && m > 0 && p0 >= 0 && p0 <= kWin;
     const uint4 vf = vflags;
     // entries: the current token of every row that selected head i, then
@@ -530,9 +530,9 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
       if (!(m > 0 && !fast_scan) && tn < ntiles) fetch(tn);
     };
     if (kPipe && one_pass)
-      qkv_entries_pipe<T, kQC, kStg>(a, ent, n_first, w, tl, m, tbase, i, u, redb, xs_dyn, ycur, ycur_ok, hook);
+      qkv_entries_pipe<T, kQC, QR, kStg>(a, ent, n_first, w, tl, m, tbase, i, u, redb, xs_dyn, ycur, ycur_ok, hook);
     else
-      qkv_entries<T, kQC>(a, ent, n_first, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok, hook);
+      qkv_entries<T, kQC, QR>(a, ent, n_first, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, ycur_ok, hook);
     if (m > 0 && !fast_scan) {
       // general path (batch > 1 or pos > 4096): windows of 4096 positions
       for (int b = 0; b < a.B; ++b) {
@@ -558,10 +558,10 @@ __global__ void __launch_bounds__(256, 2) attn_qkv_kernel(AttnArgs a, int RG, in
           }
           __syncthreads();
           if (kPipe && one_pass)
-            qkv_entries_pipe<T, kQC, kStg>(a, ent, n_ent, w, tl, m, tbase, i, u, redb, xs_dyn, ycur, false,
+            qkv_entries_pipe<T, kQC, QR, kStg>(a, ent, n_ent, w, tl, m, tbase, i, u, redb, xs_dyn, ycur, false,
                                            []() {});
           else
-            qkv_entries<T, kQC>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false, []() {});
+            qkv_entries<T, kQC, QR>(a, ent, n_ent, w, one_pass, wbase, tl, m, tbase, i, u, red, ycur, false, []() {});
         }
       }
       if (tn < ntiles) fetch(tn);
@@ -1057,8 +1057,11 @@ bool decode_width_fits(int w) {
 
 // With many (row, head) pairs the GPU is full anyway, and wider clusters
 // only add cluster barriers and co-scheduling constraints: from 64 pairs on
-// the cluster is 8 CTAs wide (each warp then takes several batches of
-// positions).  DV_DECODE_WIDTH in the environment forces a width (4..16).
+// the cluster is 8 CTAs wide, from 256 pairs 4 (each warp then takes
+// several batches of positions).  Measured at OPT-30B width, 2048
+// positions, 32 rows: 896 pairs 309 us (8 wide) and 487 us (16 wide) for
+// 941 MB, the whole attention call 528 us at 4 wide against 591 at 8.
+// DV_DECODE_WIDTH in the environment forces a width (4..16).
 template <typename T, int DH>
 int decode_cluster_width(int n_max, int pairs) {
   static const int forced = [] {
@@ -1069,6 +1072,7 @@ int decode_cluster_width(int n_max, int pairs) {
   constexpr int kPos = kDecWarps * 16;  // positions per CTA in one batch (kPW = 16)
   int want = min(kMaxCSd, max(8, (n_max + kPos - 1) / kPos));
   if (pairs >= 64) want = 8;
+  if (pairs >= 256) want = 4;
   if (decode_width_fits<T, DH>(want)) return want;
   return decode_width_fits<T, DH>(8) ? 8 : 4;
 }
@@ -1087,9 +1091,22 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
 template <typename T>
 cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t stream) {
   AttnArgs a = make_args(L, hdr);
-  // 1. projections + fused repair
-  const int tl = qkv_tpr_log2(a.d / Elem<T>::kVec);
-  const int RG = 3 * a.d_h / ((256 >> tl) * kQR);
+  // 1. projections + fused repair.  Rows of up to 768 16-byte chunks: 4 rows
+  // of 3 chunks per thread; up to 1024 chunks: 2 rows of 4; longer rows
+  // (d > 8192 for 16-bit types): 2 rows of 6 or 1 row of 8 or 10 chunks per
+  // thread, so that a row is one pass of loads and the next tile's rows are
+  // requested during the current tile's sums (4 rows of 4 chunks spilled
+  // registers, and longer rows then took two dependent passes per tile)
+  const int C = a.d / Elem<T>::kVec;
+  const bool wide = C > 256 * kQCMax;
+  const int tl = wide ? 8 : qkv_tpr_log2(C);
+  // three chunks per thread with four rows when a row fits (fewer registers,
+  // staged vectors); otherwise two rows per thread (four rows of four
+  // chunks spilled registers)
+  const bool three = !wide && C <= (1 << tl) * 3;
+  const int qc_wide = (C + 255) / 256;  // chunks per thread of a wide row (one pass)
+  const int QR = three ? kQR : (wide && qc_wide > 6 ? 1 : 2);
+  const int RG = 3 * a.d_h / ((256 >> tl) * QR);
   if (a.capU > 1024) return cudaErrorInvalidValue;
   const int tiles = a.capU * RG;
   // two resident CTAs per SM at most; no more CTAs than the largest number
@@ -1114,18 +1131,25 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
     count_launches(1);
     a.repair_only = 1;
   }
-  // single-pass rows stage their vectors in dynamic shared memory
-  const int C = a.d / Elem<T>::kVec;
-  if (C <= (1 << tl) * 3) {
+  // single-pass rows of 3 chunks stage their vectors in dynamic shared memory
+  if (wide) {
+    if (qc_wide <= 6)
+      e = launch_k(attn_qkv_kernel<T, 6, 2>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
+    else if (qc_wide <= 8)
+      e = launch_k(attn_qkv_kernel<T, 8, 1>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
+    else
+      e = launch_k(attn_qkv_kernel<T, 10, 1>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
+  } else if (three) {
     const size_t smem = qkv_stage_bytes(3);
     static PerDevice attr3;  // function attributes are per device
     const cudaError_t ea = (cudaError_t)attr3.get(current_device(), [smem] {
-      return (int)cudaFuncSetAttribute(attn_qkv_kernel<T, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      return (int)cudaFuncSetAttribute(attn_qkv_kernel<T, 3, kQR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
     });
     if (ea != cudaSuccess) return ea;
-    e = launch_k(attn_qkv_kernel<T, 3>, dim3(grid), dim3(256), smem, stream, pdl != 0, 1, a, RG, tl, pdl);
+    e = launch_k(attn_qkv_kernel<T, 3, kQR>, dim3(grid), dim3(256), smem, stream, pdl != 0, 1, a, RG, tl, pdl);
   } else {
-    e = launch_k(attn_qkv_kernel<T, 4>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
+    e = launch_k(attn_qkv_kernel<T, 4, 2>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
   }
   if (e != cudaSuccess) return e;
   if (tc) {  // the current tokens' q and K/V

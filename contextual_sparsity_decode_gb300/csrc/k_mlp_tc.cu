@@ -15,8 +15,10 @@
 //         A = gathered rows of W2n read as an MN-major operand (a neuron row
 //         is 64 contiguous columns per 128-byte swizzle row), B = a_hi and
 //         a_lo (two MMAs per K step).  Split-K over U with fp32 atomics.
-// One elected thread issues TMA loads into a ring of shared-memory stages,
-// one elected thread issues the MMAs; every wait is bounded and reports
+// Weight rows that are gathered (neurons) are copied by the CTA's four
+// epilogue warps with cp.async into the swizzled stage; rows that form a
+// tile (an attention head's block) and the small operands come by TMA from
+// one elected thread; one elected thread issues the MMAs; every wait is bounded and reports
 // DV_ERR_TIMEOUT instead of hanging.  The pipeline waits use the caller's
 // limit (dv_set_wait_limit_ns); the waits that unwind a CTA -- for the MMAs
 // it issued and for the TMA copies still landing in its shared memory --
@@ -84,16 +86,56 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// A operand rows gathered by the four epilogue warps with cp.async: thread r
+// copies its row's 128-byte segment of the stage (8 x 16 B) into the
+// 128-byte-swizzled K-major layout (16-byte chunk c of row r at chunk
+// c ^ (r % 8) of the row's 128 bytes, rows grouped by 8 in 1024-byte atoms),
+// waits for its copies S - 1 stages later, makes them visible to the async
+// proxy and arrives on the stage's barrier (count 128).  TMA gather4 moves
+// 512 bytes an instruction, which capped a CTA at ~13 GB/s on GB300.
+// warps 0-3: loaders + epilogue; warp 4: TMA producer; warp 5: MMA issuer (the
+// two single-thread roles in one warp serialised their waits: 90 against 57 us)
+constexpr int kTcThreads = 192;
+
+template <int S>
+__device__ __forceinline__ bool gather_rows_pipeline(uint8_t* sA, uint32_t stage_bytes, const uint8_t* const* src,
+                                                     const uint32_t* dst_off, int nk, uint32_t src_step,
+                                                     uint64_t* fullA, uint64_t* empty, long long wait_ns) {
+  int kb = 0, sig = 0;
+  bool ok = true;
+  for (; kb < nk; ++kb) {
+    const int st = kb % S;
+    if (kb >= S && !tc::mbar_wait(&empty[st], ((kb / S) - 1) & 1, wait_ns)) {
+      ok = false;
+      break;
+    }
+    uint8_t* base = sA + (size_t)st * stage_bytes;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cp_async16(base + dst_off[q], src[q] + (size_t)kb * src_step);
+    cp_async_commit();
+    if (kb >= S - 1) {
+      cp_async_wait<S - 1>();
+      tc::fence_proxy_async();
+      tc::mbar_arrive(&fullA[sig % S]);
+      ++sig;
+    }
+  }
+  cp_async_wait<0>();
+  tc::fence_proxy_async();
+  for (; sig < kb; ++sig) tc::mbar_arrive(&fullA[sig % S]);
+  return ok;
+}
+
 template <typename T, int BP, int EPI = kEpiMlp>
-__global__ void __launch_bounds__(128, 1)
-    mlp_tc_up_kernel(const __grid_constant__ CUtensorMap mapW1, const __grid_constant__ CUtensorMap mapY,
-                     const __grid_constant__ CUtensorMap mapT, UpArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    mlp_tc_up_kernel(const __grid_constant__ CUtensorMap mapY, const __grid_constant__ CUtensorMap mapT,
+                     const void* W, UpArgs a) {
   constexpr uint32_t kABytes = kTM * 128, kBBytes = BP * 128;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kSU], empty[kSU], done;
+  __shared__ uint64_t fullA[kSU], fullB[kSU], empty[kSU], done;
   __shared__ uint32_t tmem_base;
   __shared__ int rows[kTM];
-  __shared__ int flag_err;
+  __shared__ int issued, consumed, flag_err;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
@@ -105,7 +147,7 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSU * kABytes;
 
-  {
+  if (tid < kTM) {
     int r = a.U[min(u0 + tid, cnt - 1)];
     if (r < 0 || r >= a.N) {
       set_error(a.hdr, DV_ERR_INDEX_RANGE, r);
@@ -115,12 +157,13 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (tid == 0) {
     for (int s = 0; s < kSU; ++s) {
-      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&fullA[s], a.tile_rows ? 1 : kTM);
+      tc::mbar_init(&fullB[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(&done, 1);
     tc::fence_mbar_init();
-    flag_err = 0;
+    issued = consumed = flag_err = 0;
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
   tc::fence_before_sync();
@@ -128,115 +171,130 @@ __global__ void __launch_bounds__(128, 1)
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
   const int nk = a.d / kKB;
-  __shared__ int issued, consumed;
-  if (tid == 0) { issued = 0; consumed = 0; }
-  __syncthreads();
 
-  if (warp == 0 && lane == 0) {  // TMA producer
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kSU, it = kb / kSU;
-      if (kb >= kSU && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
-        set_error(a.hdr, DV_ERR_TIMEOUT, 1);
-        flag_err = 1;
-        break;
+  if (warp >= 4) {
+    if (warp == 4 && lane == 0) {  // TMA producer: y (and the weight rows when they form one tile)
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kSU, it = kb / kSU;
+        if (kb >= kSU && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
+          set_error(a.hdr, DV_ERR_TIMEOUT, 1);
+          flag_err = 1;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&fullB[s], kBBytes);
+        tc::tma_load_2d(sB + s * kBBytes, &mapY, kb * kKB, 0, &fullB[s]);
+        if (a.tile_rows) {
+          tc::mbar_arrive_expect_tx(&fullA[s], kABytes);
+          tc::tma_load_2d(sA + s * kABytes, &mapT, kb * kKB, rows[0], &fullA[s]);
+        }
+        issued = kb + 1;
       }
-      tc::mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
-      uint8_t* dA = sA + s * kABytes;
-      if (a.tile_rows) {
-        tc::tma_load_2d(dA, &mapT, kb * kKB, rows[0], &full[s]);
-      } else {
-#pragma unroll 4
-        for (int g = 0; g < kTM / 4; ++g)
-          tc::tma_gather4(dA + g * 512, &mapW1, kb * kKB, rows[4 * g], rows[4 * g + 1], rows[4 * g + 2],
-                          rows[4 * g + 3], &full[s]);
-      }
-      tc::tma_load_2d(sB + s * kBBytes, &mapY, kb * kKB, 0, &full[s]);
-      issued = kb + 1;
-    }
-  } else if (warp == 1 && lane == 0) {  // MMA issuer
-    constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
-    const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, false, false);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kSU, it = kb / kSU;
-      if (!tc::mbar_wait(&full[s], it & 1, a.wait_ns)) {
-        set_error(a.hdr, DV_ERR_TIMEOUT, 2);
-        flag_err = 1;
-        break;
-      }
-      tc::fence_after_sync();
-      const uint32_t aBase = tc::saddr(sA + s * kABytes), bBase = tc::saddr(sB + s * kBBytes);
+    } else if (warp == 5 && lane == 0) {  // MMA issuer
+      constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+      const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, false, false);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kSU, it = kb / kSU;
+        if (!tc::mbar_wait(&fullA[s], it & 1, a.wait_ns) || !tc::mbar_wait(&fullB[s], it & 1, a.wait_ns)) {
+          set_error(a.hdr, DV_ERR_TIMEOUT, 2);
+          flag_err = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t aBase = tc::saddr(sA + s * kABytes), bBase = tc::saddr(sB + s * kBBytes);
 #pragma unroll
-      for (int kk = 0; kk < kKB / 16; ++kk) {
-        const uint64_t ad = tc::smem_desc(aBase + kk * 32, 16, 1024, 2);
-        const uint64_t bd = tc::smem_desc(bBase + kk * 32, 16, 1024, 2);
-        tc::mma_f16(tmem, ad, bd, idesc, (kb | kk) != 0);
+        for (int kk = 0; kk < kKB / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc(aBase + kk * 32, 16, 1024, 2);
+          const uint64_t bd = tc::smem_desc(bBase + kk * 32, 16, 1024, 2);
+          tc::mma_f16(tmem, ad, bd, idesc, (kb | kk) != 0);
+        }
+        tc::mma_commit(&empty[s]);
+        consumed = kb + 1;
       }
-      tc::mma_commit(&empty[s]);
-      consumed = kb + 1;
+      tc::mma_commit(&done);  // arrives once every issued MMA has completed
     }
-    tc::mma_commit(&done);  // arrives once every issued MMA has completed
+    __syncwarp();
+  } else if (!a.tile_rows) {  // warps 0-3 gather the weight rows
+    const uint8_t* src[8];
+    uint32_t off[8];
+    const T* row = static_cast<const T*>(W) + (size_t)rows[tid] * a.d;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      src[q] = reinterpret_cast<const uint8_t*>(row + q * 8);
+      off[q] = (uint32_t)((tid >> 3) * 1024 + (tid & 7) * 128 + ((q ^ (tid & 7)) << 4));
+    }
+    if (!gather_rows_pipeline<kSU>(sA, kABytes, src, off, nk, kKB * sizeof(T), fullA, empty, a.wait_ns)) {
+      set_error(a.hdr, DV_ERR_TIMEOUT, 7);
+      flag_err = 1;
+    }
   }
-  __syncwarp();
 
-  // epilogue: thread = accumulator row (neuron u0 + tid)
-  const bool ok = tc::mbar_wait(&done, 0, unwind_ns);
-  if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 3);
-  __syncwarp();
-  tc::fence_after_sync();
+  // epilogue (warps 0-3): thread = accumulator row (union entry u0 + tid)
+  bool ok = true;
   float v[BP];
+  if (tid < kTM) {
+    ok = tc::mbar_wait(&done, 0, unwind_ns);
+    if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 3);
+    __syncwarp();
+    tc::fence_after_sync();
 #pragma unroll
-  for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
-  tc::tmem_ld_wait();
-  const int u = u0 + tid;
-  const bool live = ok && !flag_err && u < cnt;
-  const int row = rows[tid];
-  if (EPI == kEpiMlp) {
-    T* hi = static_cast<T*>(a.act_hi);
-    T* lo = static_cast<T*>(a.act_lo);
+    for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
+    tc::tmem_ld_wait();
+  }
+  __syncthreads();  // flag_err is final
+  if (tid < kTM) {
+    const int u = u0 + tid;
+    const bool live = ok && !flag_err && u < cnt;
+    const int row = rows[tid];
+    if (EPI == kEpiMlp) {
+      T* hi = static_cast<T*>(a.act_hi);
+      T* lo = static_cast<T*>(a.act_lo);
 #pragma unroll
-    for (int b = 0; b < BP; ++b) {
-      float x = fmaxf(v[b], 0.f);
-      if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
-      const T h = Elem<T>::from_f(x);
-      const T l = Elem<T>::from_f(x - Elem<T>::to_f(h));
-      hi[(size_t)b * a.Upad + u] = h;
-      lo[(size_t)b * a.Upad + u] = l;
-    }
-  } else if (live) {
-    const int dh3 = 3 * a.d_h;
-    const int i = row / dh3, rem = row - i * dh3, m = rem / a.d_h, t = rem - m * a.d_h;
-    const int slot = m == 0 ? a.slot_of[i] : 0;
-    T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
+      for (int b = 0; b < BP; ++b) {
+        float x = fmaxf(v[b], 0.f);
+        if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
+        const T h = Elem<T>::from_f(x);
+        const T l = Elem<T>::from_f(x - Elem<T>::to_f(h));
+        hi[(size_t)b * a.Upad + u] = h;
+        lo[(size_t)b * a.Upad + u] = l;
+      }
+    } else if (live) {
+      const int dh3 = 3 * a.d_h;
+      const int i = row / dh3, rem = row - i * dh3, m = rem / a.d_h, t = rem - m * a.d_h;
+      const int slot = m == 0 ? a.slot_of[i] : 0;
+      T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
 #pragma unroll
-    for (int b = 0; b < BP; ++b) {
-      if (b >= a.B || !bit_test(a.member + (size_t)b * a.words, i)) continue;
-      if (m == 0) {
-        a.q[((size_t)b * a.capQ + slot) * a.d_h + t] = v[b];
-      } else {
-        const int p = a.pos[b];
-        if (p >= 0 && p < a.n_max) dst[(((size_t)b * a.h + i) * a.n_max + p) * a.d_h + t] = Elem<T>::from_f(v[b]);
+      for (int b = 0; b < BP; ++b) {
+        if (b >= a.B || !bit_test(a.member + (size_t)b * a.words, i)) continue;
+        if (m == 0) {
+          a.q[((size_t)b * a.capQ + slot) * a.d_h + t] = v[b];
+        } else {
+          const int p = a.pos[b];
+          if (p >= 0 && p < a.n_max) dst[(((size_t)b * a.h + i) * a.n_max + p) * a.d_h + t] = Elem<T>::from_f(v[b]);
+        }
       }
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  // make sure no TMA write into this CTA's shared memory is still in flight
+  // no TMA write into this CTA's shared memory may still be in flight (the
+  // loaders waited for their own copies)
   if (tid == 0) {
-    for (int kb = consumed; kb < issued; ++kb)
-      if (!tc::mbar_wait(&full[kb % kSU], (kb / kSU) & 1, unwind_ns)) break;
+    for (int kb = consumed; kb < issued; ++kb) {
+      if (!tc::mbar_wait(&fullB[kb % kSU], (kb / kSU) & 1, unwind_ns)) break;
+      if (a.tile_rows && !tc::mbar_wait(&fullA[kb % kSU], (kb / kSU) & 1, unwind_ns)) break;
+    }
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <typename T, int BP>
-__global__ void __launch_bounds__(128, 1)
-    mlp_tc_down_kernel(const __grid_constant__ CUtensorMap mapW2, const __grid_constant__ CUtensorMap mapHi,
-                       const __grid_constant__ CUtensorMap mapLo, const __grid_constant__ CUtensorMap mapT,
-                       DownArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    mlp_tc_down_kernel(const __grid_constant__ CUtensorMap mapHi, const __grid_constant__ CUtensorMap mapLo,
+                       const __grid_constant__ CUtensorMap mapT, const void* W, DownArgs a) {
   constexpr uint32_t kABytes = kKB * 256, kBBytes = BP * 128;  // A: 64 neurons x 128 columns
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kSD], empty[kSD], done;
+  __shared__ uint64_t fullA[kSD], fullB[kSD], empty[kSD], done;
   __shared__ uint32_t tmem_base;
   __shared__ int rows[kKChunk];
   __shared__ int issued, consumed, flag_err;
@@ -265,7 +323,8 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (tid == 0) {
     for (int s = 0; s < kSD; ++s) {
-      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&fullA[s], a.tile_rows ? 1 : kTM);
+      tc::mbar_init(&fullB[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(&done, 1);
@@ -278,79 +337,110 @@ __global__ void __launch_bounds__(128, 1)
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
 
-  if (warp == 0 && lane == 0) {  // TMA producer
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kSD, it = kb / kSD;
-      if (kb >= kSD && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
-        set_error(a.hdr, DV_ERR_TIMEOUT, 4);
-        flag_err = 1;
+  if (warp >= 4) {
+    if (warp == 4 && lane == 0) {  // TMA producer: the coefficient halves (and the rows when they form tiles)
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kSD, it = kb / kSD;
+        if (kb >= kSD && !tc::mbar_wait(&empty[s], (it - 1) & 1, a.wait_ns)) {
+          set_error(a.hdr, DV_ERR_TIMEOUT, 4);
+          flag_err = 1;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&fullB[s], 2 * kBBytes);
+        tc::tma_load_2d(sH + s * kBBytes, &mapHi, k0 + kb * kKB, 0, &fullB[s]);
+        tc::tma_load_2d(sL + s * kBBytes, &mapLo, k0 + kb * kKB, 0, &fullB[s]);
+        if (a.tile_rows) {
+          const int r0 = rows[kb * kKB];
+          tc::mbar_arrive_expect_tx(&fullA[s], kABytes);
+          tc::tma_load_2d(sA + s * kABytes, &mapT, c0, r0, &fullA[s]);
+          tc::tma_load_2d(sA + s * kABytes + kKB * 128, &mapT, c0 + 64, r0, &fullA[s]);
+        }
+        issued = kb + 1;
+      }
+    } else if (warp == 5 && lane == 0) {  // MMA issuer
+      constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+      const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, /*A MN-major*/ true, false);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kSD, it = kb / kSD;
+        if (!tc::mbar_wait(&fullA[s], it & 1, a.wait_ns) || !tc::mbar_wait(&fullB[s], it & 1, a.wait_ns)) {
+          set_error(a.hdr, DV_ERR_TIMEOUT, 5);
+          flag_err = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t aBase = tc::saddr(sA + s * kABytes);
+        const uint32_t hBase = tc::saddr(sH + s * kBBytes), lBase = tc::saddr(sL + s * kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKB / 16; ++kk) {
+          // A (MN-major): 16 neuron rows = two 8-row groups (1024 B apart);
+          // the two 64-column halves of the tile are kKB*128 bytes apart
+          const uint64_t ad = tc::smem_desc(aBase + kk * 2048, kKB * 128, 1024, 2);
+          const uint64_t hd = tc::smem_desc(hBase + kk * 32, 16, 1024, 2);
+          const uint64_t ld = tc::smem_desc(lBase + kk * 32, 16, 1024, 2);
+          tc::mma_f16(tmem, ad, hd, idesc, (kb | kk) != 0);
+          tc::mma_f16(tmem, ad, ld, idesc, 1);
+        }
+        tc::mma_commit(&empty[s]);
+        consumed = kb + 1;
+      }
+      tc::mma_commit(&done);
+    }
+    __syncwarp();
+  } else if (!a.tile_rows) {  // warps 0-3 gather the weight rows: thread = (row r, column half)
+    const int r = tid & (kKB - 1), half = tid >> 6;
+    // row r of stage kb is rows[kb * kKB + r]: a new row every stage
+    int kb = 0, sig = 0;
+    bool okl = true;
+    for (; kb < nk; ++kb) {
+      const int st = kb % kSD;
+      if (kb >= kSD && !tc::mbar_wait(&empty[st], ((kb / kSD) - 1) & 1, a.wait_ns)) {
+        okl = false;
         break;
       }
-      tc::mbar_arrive_expect_tx(&full[s], kABytes + 2 * kBBytes);
-      uint8_t* dA = sA + s * kABytes;
-      const int* rr = rows + kb * kKB;
-      if (a.tile_rows) {
-        tc::tma_load_2d(dA, &mapT, c0, rr[0], &full[s]);
-        tc::tma_load_2d(dA + kKB * 128, &mapT, c0 + 64, rr[0], &full[s]);
-      } else {
+      const T* rowp = static_cast<const T*>(W) + (size_t)rows[kb * kKB + r] * a.d + c0 + half * 64;
+      uint8_t* base = sA + (size_t)st * kABytes + half * (kKB * 128) + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll 4
-          for (int g = 0; g < kKB / 4; ++g)
-            tc::tma_gather4(dA + half * (kKB * 128) + g * 512, &mapW2, c0 + half * 64, rr[4 * g], rr[4 * g + 1],
-                            rr[4 * g + 2], rr[4 * g + 3], &full[s]);
+      for (int q = 0; q < 8; ++q) cp_async16(base + ((q ^ (r & 7)) << 4), rowp + q * 8);
+      cp_async_commit();
+      if (kb >= kSD - 1) {
+        cp_async_wait<kSD - 1>();
+        tc::fence_proxy_async();
+        tc::mbar_arrive(&fullA[sig % kSD]);
+        ++sig;
       }
-      tc::tma_load_2d(sH + s * kBBytes, &mapHi, k0 + kb * kKB, 0, &full[s]);
-      tc::tma_load_2d(sL + s * kBBytes, &mapLo, k0 + kb * kKB, 0, &full[s]);
-      issued = kb + 1;
     }
-  } else if (warp == 1 && lane == 0) {  // MMA issuer
-    constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
-    const uint32_t idesc = tc::idesc_f16(kTM, BP, kBf16, /*A MN-major*/ true, false);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kSD, it = kb / kSD;
-      if (!tc::mbar_wait(&full[s], it & 1, a.wait_ns)) {
-        set_error(a.hdr, DV_ERR_TIMEOUT, 5);
-        flag_err = 1;
-        break;
-      }
-      tc::fence_after_sync();
-      const uint32_t aBase = tc::saddr(sA + s * kABytes);
-      const uint32_t hBase = tc::saddr(sH + s * kBBytes), lBase = tc::saddr(sL + s * kBBytes);
-#pragma unroll
-      for (int kk = 0; kk < kKB / 16; ++kk) {
-        // A (MN-major): 16 neuron rows = two 8-row groups (1024 B apart);
-        // the two 64-column halves of the tile are kKB*128 bytes apart
-        const uint64_t ad = tc::smem_desc(aBase + kk * 2048, kKB * 128, 1024, 2);
-        const uint64_t hd = tc::smem_desc(hBase + kk * 32, 16, 1024, 2);
-        const uint64_t ld = tc::smem_desc(lBase + kk * 32, 16, 1024, 2);
-        tc::mma_f16(tmem, ad, hd, idesc, (kb | kk) != 0);
-        tc::mma_f16(tmem, ad, ld, idesc, 1);
-      }
-      tc::mma_commit(&empty[s]);
-      consumed = kb + 1;
+    cp_async_wait<0>();
+    tc::fence_proxy_async();
+    for (; sig < kb; ++sig) tc::mbar_arrive(&fullA[sig % kSD]);
+    if (!okl) {
+      set_error(a.hdr, DV_ERR_TIMEOUT, 8);
+      flag_err = 1;
     }
-    tc::mma_commit(&done);
   }
-  __syncwarp();
 
-  const bool ok = tc::mbar_wait(&done, 0, unwind_ns);
-  if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 6);
-  __syncwarp();
-  tc::fence_after_sync();
+  bool ok = true;
   float v[BP];
+  if (tid < kTM) {
+    ok = tc::mbar_wait(&done, 0, unwind_ns);
+    if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 6);
+    __syncwarp();
+    tc::fence_after_sync();
 #pragma unroll
-  for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
-  tc::tmem_ld_wait();
-  if (ok && !flag_err) {
+    for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
+    tc::tmem_ld_wait();
+  }
+  __syncthreads();  // flag_err is final
+  if (tid < kTM && ok && !flag_err) {
     const int col = c0 + tid;
     for (int b = 0; b < a.B; ++b) atomicAdd(a.out + (size_t)b * a.d + col, v[b]);
   }
   tc::fence_before_sync();
   __syncthreads();
   if (tid == 0) {
-    for (int kb = consumed; kb < issued; ++kb)
-      if (!tc::mbar_wait(&full[kb % kSD], (kb / kSD) & 1, unwind_ns)) break;
+    for (int kb = consumed; kb < issued; ++kb) {
+      if (!tc::mbar_wait(&fullB[kb % kSD], (kb / kSD) & 1, unwind_ns)) break;
+      if (a.tile_rows && !tc::mbar_wait(&fullA[kb % kSD], (kb / kSD) & 1, unwind_ns)) break;
+    }
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -394,9 +484,8 @@ template <typename T, int BP>
 cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   constexpr bool bf16 = !std::is_same<T, __half>::value;
   const int Upad = tc_act_cols(L.N);
-  CUtensorMap mW1, mW2, mY, mHi, mLo;
-  if (!make_map(&mW1, L.W1n, L.d, L.N, 1, bf16) || !make_map(&mW2, L.W2n, L.d, L.N, 1, bf16) ||
-      !make_map(&mY, L.y, L.d, L.B, BP, bf16) || !make_map(&mHi, L.act_hi, Upad, BP, BP, bf16) ||
+  CUtensorMap mY, mHi, mLo;
+  if (!make_map(&mY, L.y, L.d, L.B, BP, bf16) || !make_map(&mHi, L.act_hi, Upad, BP, BP, bf16) ||
       !make_map(&mLo, L.act_lo, Upad, BP, BP, bf16))
     return cudaErrorInvalidValue;
   const size_t smem_up = 1024 + kSU * (kTM * 128 + BP * 128);
@@ -414,12 +503,13 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   const int maxU = L.N < L.B * L.cap ? L.N : L.B * L.cap;
   UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr,
             wait_limit_ns()};
-  mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, 128, smem_up, stream>>>(mW1, mY, mW1, ua);
+  // neuron rows are gathered by the CTAs' own threads (mapT is not used)
+  mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, kTcThreads, smem_up, stream>>>(mY, mY, L.W1n, ua);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr, wait_limit_ns()};
   dim3 g(L.d / kTM, (maxU + kKChunk - 1) / kKChunk);
-  mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW2, mHi, mLo, mW2, da);
+  mlp_tc_down_kernel<T, BP><<<g, kTcThreads, smem_dn, stream>>>(mHi, mLo, mHi, L.W2n, da);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(2);
   return e;
@@ -429,9 +519,8 @@ template <typename T, int BP>
 cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   constexpr bool bf16 = !std::is_same<T, __half>::value;
   const int nrows = L.h * 3 * L.d_h;
-  CUtensorMap mW, mY, mT;
-  if (!make_map(&mW, L.Wqkv, L.d, nrows, 1, bf16) || !make_map(&mY, L.y, L.d, L.B, BP, bf16) ||
-      !make_map(&mT, L.Wqkv, L.d, nrows, kTM, bf16))
+  CUtensorMap mY, mT;
+  if (!make_map(&mY, L.y, L.d, L.B, BP, bf16) || !make_map(&mT, L.Wqkv, L.d, nrows, kTM, bf16))
     return cudaErrorInvalidValue;
   const size_t smem_up = 1024 + kSU * (kTM * 128 + BP * 128);
   static PerDevice attr;  // function attributes are per device
@@ -448,7 +537,8 @@ cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream)
   // a head's 3 d_h rows are contiguous: with d_h = 128 every 128-row tile is
   // one head's Q, K or V block
   ua.tile_rows = (3 * L.d_h) % kTM == 0 ? 1 : 0;
-  mlp_tc_up_kernel<T, BP, kEpiQkv><<<(L.max_rows + kTM - 1) / kTM, 128, smem_up, stream>>>(mW, mY, mT, ua);
+  mlp_tc_up_kernel<T, BP, kEpiQkv><<<(L.max_rows + kTM - 1) / kTM, kTcThreads, smem_up, stream>>>(mY, mT, L.Wqkv,
+                                                                                                   ua);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(1);
   return e;
@@ -457,9 +547,9 @@ cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream)
 template <typename T, int BP>
 cudaError_t run_rows_tc(const TcRowsLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   constexpr bool bf16 = !std::is_same<T, __half>::value;
-  CUtensorMap mW, mHi, mLo, mT;
-  if (!make_map(&mW, L.W, L.d, L.n_rows, 1, bf16) || !make_map(&mHi, L.act_hi, L.Upad, BP, BP, bf16) ||
-      !make_map(&mLo, L.act_lo, L.Upad, BP, BP, bf16) || !make_map(&mT, L.W, L.d, L.n_rows, kKB, bf16))
+  CUtensorMap mHi, mLo, mT;
+  if (!make_map(&mHi, L.act_hi, L.Upad, BP, BP, bf16) || !make_map(&mLo, L.act_lo, L.Upad, BP, BP, bf16) ||
+      !make_map(&mT, L.W, L.d, L.n_rows, kKB, bf16))
     return cudaErrorInvalidValue;
   const size_t smem_dn = 1024 + kSD * (kKB * 256 + 2 * BP * 128);
   static PerDevice attr;  // function attributes are per device
@@ -471,7 +561,7 @@ cudaError_t run_rows_tc(const TcRowsLaunch& L, WsHeader* hdr, cudaStream_t strea
   DownArgs da{L.rows, L.rows_count, L.n_rows, L.B, L.d, L.n_rows, L.out, hdr, wait_limit_ns(),
               L.rows_per_unit % kKB == 0 ? 1 : 0};
   dim3 g(L.d / kTM, (L.max_rows + kKChunk - 1) / kKChunk);
-  mlp_tc_down_kernel<T, BP><<<g, 128, smem_dn, stream>>>(mW, mHi, mLo, mT, da);
+  mlp_tc_down_kernel<T, BP><<<g, kTcThreads, smem_dn, stream>>>(mHi, mLo, mT, L.W, da);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(1);
   return e;

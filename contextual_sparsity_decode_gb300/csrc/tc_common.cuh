@@ -50,6 +50,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 
+// Make this thread's earlier generic-proxy writes to shared memory (plain
+// stores, and cp.async copies it has waited for) visible to the async proxy
+// (tcgen05.mma operand reads, TMA).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---- TMA ----------------------------------------------------------------------
 
 // Contiguous global -> shared copy (addresses 16-byte aligned, size a multiple

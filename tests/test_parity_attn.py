@@ -39,6 +39,11 @@ CASES = [
     ("random_sizes_f16", 2, 256,  8,  64,  "f16",  [9, 4],        48,   8,    "rnd", "isq",  None),
     ("random_sizes_b1",  1, 384,  12, 64,  "f16",  [21],          48,   12,   "rnd", "isq",  None),
     ("opt13b_b1_bf16",   1, 5120, 40, 128, "bf16", [300],         320,  2,    12,    "isq",  0.02),
+    # long projection rows: 2 rows of 4 chunks, 2 of 6, 1 of 8 or 10 per thread
+    ("rows4x2_bf16_7k",  1, 7168, 4,  128, "bf16", [33],          48,   4,    2,     "isq",  0.02),
+    ("wide_f32_8k",      1, 8192, 4,  64,  "f32",  [40],          64,   3,    2,     "isq",  None),
+    ("wide_f16_16k",     2, 16384, 4, 128, "f16",  [30, 17],      48,   3,    2,     "isq",  0.02),
+    ("wide_f16_20k",     1, 20480, 2, 64,  "f16",  [20],          32,   3,    1,     "isq",  0.02),
     # 8+ rows of a 16-bit type: projections and output projection on the tensor cores,
     # repairs of skipped heads planned per (row, head)
     ("batch16_f16_tc",   16, 512, 8,  64,  "f16",  [20 + b for b in range(16)], 64, 6, 3, "isq", None),
