@@ -153,6 +153,11 @@ cudaError_t launch_rows_tc(const TcRowsLaunch& a, dv_dtype dt, WsHeader* hdr, cu
 // Batch 1, streaming pass over the selected rows with bulk copies into a
 // shared-memory ring (k_stream.cu); adds into out with atomics.
 bool mlp_stream_supported(int d, dv_dtype dt);
+// Batch 1: out += sum_u sum_t coef[u][t] W[units[u] * rpu + t] streamed the
+// same way (the attention output projection of long rows).
+cudaError_t launch_rows_stream(const void* W, const int32_t* units, const int32_t* n_units, int cap,
+                               int n_rows_units, int rpu, int d, const float* coef, dv_dtype dt, float* out,
+                               WsHeader* hdr, int num_sms, cudaStream_t stream);
 cudaError_t launch_mlp_stream(const void* y, int d, int N, const void* W1n, const void* W2n,
                               const int32_t* list, const int32_t* count, int cap, dv_dtype dt, float* out,
                               WsHeader* hdr, int num_sms, int pdl, cudaStream_t stream);

@@ -1088,6 +1088,19 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream) {
   return a.d_h == 128 ? launch_decode_dh<T, 128>(a, stream) : launch_decode_dh<T, 64>(a, stream);
 }
 
+// Batch-1 output projection as a streaming pass when the selected W^O rows
+// amount to at least 48 MB (OPT-175B-shaped: 63 MB; the column-sliced
+// combine reached ~2 TB/s there).  DV_ATTN_STREAM=1 or 0 in the environment
+// forces it on or off.
+bool use_rows_stream(size_t bytes) {
+  static const int forced = [] {
+    const char* e = getenv("DV_ATTN_STREAM");
+    return e ? atoi(e) : -1;
+  }();
+  if (forced >= 0) return forced != 0;
+  return bytes >= (size_t)48 << 20;
+}
+
 template <typename T>
 cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t stream) {
   AttnArgs a = make_args(L, hdr);
@@ -1200,6 +1213,15 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   c.coef = a.H; c.coef_stride = (size_t)a.capU * a.d_h;
   c.member = a.member; c.words = a.hwords;
   c.B = a.B; c.out = L.out; c.accumulate = L.accumulate; c.hdr = hdr;
+  if (a.B == 1 && use_rows_stream((size_t)a.cap * a.d_h * a.d * sizeof(T))) {
+    // long selections of long rows: stream the W^O rows (see k_stream.cu)
+    if (!L.accumulate) {
+      e = cudaMemsetAsync(L.out, 0, (size_t)a.d * sizeof(float), stream);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_rows_stream(L.Wo, a.U, a.U_count, a.capU, a.h, a.d_h, a.d, a.H, dtype_of<T>(), L.out, hdr,
+                              num_sms, stream);
+  }
   return launch_rows_combine(c, dtype_of<T>(), stream);
 }
 

@@ -86,13 +86,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// A operand rows gathered by the four epilogue warps with cp.async: thread r
-// copies its row's 128-byte segment of the stage (8 x 16 B) into the
-// 128-byte-swizzled K-major layout (16-byte chunk c of row r at chunk
-// c ^ (r % 8) of the row's 128 bytes, rows grouped by 8 in 1024-byte atoms),
-// waits for its copies S - 1 stages later, makes them visible to the async
-// proxy and arrives on the stage's barrier (count 128).  TMA gather4 moves
-// 512 bytes an instruction, which capped a CTA at ~13 GB/s on GB300.
+// A operand rows gathered by the four epilogue warps with cp.async: each
+// thread copies eight 16-byte chunks of the stage into the 128-byte-swizzled
+// K-major layout (16-byte chunk c of row r at chunk c ^ (r % 8) of the row's
+// 128 bytes, rows grouped by 8 in 1024-byte atoms), waits for its copies
+// S - 1 stages later, makes them visible to the async proxy and arrives on
+// the stage's barrier (count 128).  TMA gather4 moves 512 bytes an
+// instruction, which capped a CTA at ~13 GB/s on GB300.
 // warps 0-3: loaders + epilogue; warp 4: TMA producer; warp 5: MMA issuer (the
 // two single-thread roles in one warp serialised their waits: 90 against 57 us)
 constexpr int kTcThreads = 192;
@@ -214,13 +214,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (!a.tile_rows) {  // warps 0-3 gather the weight rows
+    // thread t copies 16-byte chunk t % 8 of rows t / 8 + 16 q (q < 8): eight
+    // lanes cover one row's 128 bytes, so a warp instruction reads four whole
+    // 128-byte lines (a row per lane touched 32 lines: ~2.1 TB/s)
     const uint8_t* src[8];
     uint32_t off[8];
-    const T* row = static_cast<const T*>(W) + (size_t)rows[tid] * a.d;
+    const int ch = tid & 7;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      src[q] = reinterpret_cast<const uint8_t*>(row + q * 8);
-      off[q] = (uint32_t)((tid >> 3) * 1024 + (tid & 7) * 128 + ((q ^ (tid & 7)) << 4));
+      const int r = (tid >> 3) + 16 * q;
+      src[q] = reinterpret_cast<const uint8_t*>(static_cast<const T*>(W) + (size_t)rows[r] * a.d + ch * 8);
+      off[q] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4));
     }
     if (!gather_rows_pipeline<kSU>(sA, kABytes, src, off, nk, kKB * sizeof(T), fullA, empty, a.wait_ns)) {
       set_error(a.hdr, DV_ERR_TIMEOUT, 7);
@@ -387,8 +391,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (!a.tile_rows) {  // warps 0-3 gather the weight rows: thread = (row r, column half)
-    const int r = tid & (kKB - 1), half = tid >> 6;
-    // row r of stage kb is rows[kb * kKB + r]: a new row every stage
+    // thread t copies 16-byte chunk t % 8 of the 128-byte segments
+    // g = t / 8 + 16 q (q < 8) of the stage: segment g is column half g / 64
+    // of neuron row g % 64 (eight lanes per segment: whole lines per warp
+    // instruction); the rows change every stage
+    const int ch = tid & 7;
     int kb = 0, sig = 0;
     bool okl = true;
     for (; kb < nk; ++kb) {
@@ -397,10 +404,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         okl = false;
         break;
       }
-      const T* rowp = static_cast<const T*>(W) + (size_t)rows[kb * kKB + r] * a.d + c0 + half * 64;
-      uint8_t* base = sA + (size_t)st * kABytes + half * (kKB * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t* base = sA + (size_t)st * kABytes;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) cp_async16(base + ((q ^ (r & 7)) << 4), rowp + q * 8);
+      for (int q = 0; q < 8; ++q) {
+        const int g = (tid >> 3) + 16 * q, r = g & (kKB - 1), half = g >> 6;
+        const T* src = static_cast<const T*>(W) + (size_t)rows[kb * kKB + r] * a.d + c0 + half * 64 + ch * 8;
+        cp_async16(base + half * (kKB * 128) + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4), src);
+      }
       cp_async_commit();
       if (kb >= kSD - 1) {
         cp_async_wait<kSD - 1>();
