@@ -258,8 +258,10 @@ def _block_bytes(w, B, mean_n, uA, uM, sumA):
 KNAMES = {"mlp": "dv_sparse_mlp", "attn": "dv_sparse_attn", "predict": "dv_predict",
           "ln": "dv_layernorm"}
 KERNELS = {"mlp": "mlp_fused_kernel (batch 1; else union + up + combine, or union + tcgen05 up/down)",
-           "attn": "attn_qkv_kernel + attn_decode_kernel + rows_combine_kernel",
-           "predict": "rows_dot x2 + select_kernel", "ln": "layernorm_kernel"}
+           "attn": "attn_qkv_kernel + attn_decode_kernel + rows_combine_kernel "
+                   "(8+ rows: repair plan + tcgen05 q/K/V + decode + tcgen05 output projection)",
+           "predict": "rows_dot x2 + select_kernel (8+ rows: pred_tc_kernel x2 + select_kernel)",
+           "ln": "layernorm_kernel"}
 
 
 def _union_sizes(dec):

@@ -64,12 +64,18 @@ constexpr int kMaxB = 32;
 struct PredWs {
   float* h[2];
   float* s[2];
+  uint16_t* h_hi[2];
+  uint16_t* h_lo[2];
 };
 PredWs carve_pred(Carver& c, int B, int n_preds, const int* r, const int* N) {
   PredWs w{};
   for (int i = 0; i < n_preds; ++i) {
     w.h[i] = c.take<float>((size_t)B * r[i]);
     w.s[i] = c.take<float>((size_t)B * N[i]);
+    if (B >= kTcMinBatch) {  // tensor-core path: h as two 16-bit halves, 32 rows
+      w.h_hi[i] = c.take<uint16_t>((size_t)32 * r[i]);
+      w.h_lo[i] = c.take<uint16_t>((size_t)32 * r[i]);
+    }
   }
   return w;
 }
@@ -298,6 +304,8 @@ dv_status dv_predict(const void* y, int B, int d, dv_dtype dt, const dv_predicto
     L.mode[i] = (int)p.mode; L.k[i] = p.k; L.t[i] = p.t;
     L.idx[i] = p.idx; L.cap[i] = p.cap; L.count[i] = p.count;
     L.h[i] = w.h[i];
+    L.h_hi[i] = w.h_hi[i];
+    L.h_lo[i] = w.h_lo[i];
     L.s[i] = p.scores ? p.scores : w.s[i];
   }
   cudaError_t e = launch_predict(y, B, d, dt, L, n_preds, static_cast<WsHeader*>(ws), stream);

@@ -88,11 +88,19 @@ struct PredLaunch {
   int32_t* count[2];
   float* h[2];       // [B][r] fp32 scratch
   float* s[2];       // [B][N] fp32 scores (caller buffer or scratch)
+  void* h_hi[2];     // tensor-core path: [32][r] storage-type halves of h,
+  void* h_lo[2];     // or null (then the CUDA-core path runs)
 };
 
 cudaError_t launch_predict(const void* y, int B, int d, dv_dtype dt,
                            const PredLaunch& p, int n_preds, WsHeader* hdr,
                            cudaStream_t stream);
+
+// Both products of the predictor for 8..32 rows on tcgen05 (k_predict_tc.cu):
+// scores into p.s; the selection is launched by launch_predict.
+bool predict_tc_supported(int B, int d, dv_dtype dt, const PredLaunch& p, int n_preds);
+cudaError_t launch_predict_tc(const void* y, int B, int d, dv_dtype dt, const PredLaunch& p, int n_preds,
+                              WsHeader* hdr, cudaStream_t stream);
 
 // ---- sparse MLP (k_mlp.cu) ---------------------------------------------------
 

@@ -5,6 +5,8 @@
 // Launch 1 (rows_dot<ReLU>):    h = ReLU(y P1)       both predictors
 // Launch 2 (rows_dot<Sigmoid>): s = sigmoid(h P2)    both predictors
 // Launch 3 (select_kernel):     index lists, one CTA per (predictor, row)
+// Batches of 8..32 rows in 16-bit types run launches 1 and 2 on the tensor
+// cores instead (k_predict_tc.cu).
 //
 // Both GEMVs are HBM-bound row streams.  A CTA owns a tile of rows; a group
 // of TPR threads (32..256) shares one row, each thread holding up to kC
@@ -404,6 +406,25 @@ cudaError_t run_rows(RowArgs a, cudaStream_t stream) {
   return cudaSuccess;
 }
 
+// One CTA per (row, predictor): top-k or threshold over the fp32 scores.
+cudaError_t select_all(int B, const PredLaunch& p, int n_preds, WsHeader* hdr, cudaStream_t stream) {
+  SelArgs sa{};
+  int nmax = 0;
+  for (int i = 0; i < n_preds; ++i) {
+    sa.s[i] = p.s[i]; sa.N[i] = p.N[i]; sa.mode[i] = p.mode[i]; sa.k[i] = p.k[i];
+    sa.cap[i] = p.cap[i]; sa.t[i] = p.t[i]; sa.idx[i] = p.idx[i]; sa.count[i] = p.count[i];
+    nmax = p.N[i] > nmax ? p.N[i] : nmax;
+  }
+  const size_t smem = (size_t)nmax * sizeof(uint32_t);
+  static PerDevice attr;  // function attributes are per device
+  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [] {
+    return (int)cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kSelectMaxN * sizeof(uint32_t)));
+  });
+  if (ea != cudaSuccess) return ea;
+  return launch_k(select_kernel, dim3(B, n_preds), dim3(kSelThreads), smem, stream, true, 1, sa, hdr);
+}
+
 template <typename T>
 cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_preds,
                       WsHeader* hdr, cudaStream_t stream) {
@@ -421,22 +442,7 @@ cudaError_t predict_t(const void* y, int B, int d, const PredLaunch& p, int n_pr
   for (int i = 0; i < n_preds; ++i) g2.seg[i] = RowSeg{p.P2t[i], p.h[i], p.s[i], p.N[i], p.r[i], 0, 0};
   e = run_rows<T, float, kSigmoid>(g2, stream);
   if (e != cudaSuccess) return e;
-
-  SelArgs sa{};
-  int nmax = 0;
-  for (int i = 0; i < n_preds; ++i) {
-    sa.s[i] = p.s[i]; sa.N[i] = p.N[i]; sa.mode[i] = p.mode[i]; sa.k[i] = p.k[i];
-    sa.cap[i] = p.cap[i]; sa.t[i] = p.t[i]; sa.idx[i] = p.idx[i]; sa.count[i] = p.count[i];
-    nmax = p.N[i] > nmax ? p.N[i] : nmax;
-  }
-  const size_t smem = (size_t)nmax * sizeof(uint32_t);
-  static PerDevice attr;  // function attributes are per device
-  const cudaError_t ea = (cudaError_t)attr.get(current_device(), [] {
-    return (int)cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(kSelectMaxN * sizeof(uint32_t)));
-  });
-  if (ea != cudaSuccess) return ea;
-  return launch_k(select_kernel, dim3(B, n_preds), dim3(kSelThreads), smem, stream, true, 1, sa, hdr);
+  return select_all(B, p, n_preds, hdr, stream);
 }
 
 }  // namespace
@@ -458,6 +464,10 @@ cudaError_t launch_select(const float* scores, int B, int N, int mode, int k, fl
 
 cudaError_t launch_predict(const void* y, int B, int d, dv_dtype dt, const PredLaunch& p,
                            int n_preds, WsHeader* hdr, cudaStream_t stream) {
+  if (predict_tc_supported(B, d, dt, p, n_preds)) {
+    const cudaError_t e = launch_predict_tc(y, B, d, dt, p, n_preds, hdr, stream);
+    return e != cudaSuccess ? e : select_all(B, p, n_preds, hdr, stream);
+  }
   switch (dt) {
     case DV_F32: return predict_t<float>(y, B, d, p, n_preds, hdr, stream);
     case DV_F16: return predict_t<__half>(y, B, d, p, n_preds, hdr, stream);

@@ -33,6 +33,11 @@ CASES = [
     ("kN_f16",                   1, 256,   64,   500,   "f16",  "topk",     500,  0.5),
     ("batch8_f16",               8, 1024,  256,  4096,  "f16",  "topk",     205,  0.5),
     ("batch32_bf16",             32, 1024, 256,  4096,  "bf16", "topk",     205,  0.5),
+    # tensor-core predictor (8..32 rows): ragged rows, r and d off the tiles
+    ("batch13_ragged_f16",       13, 1032, 200,  3000,  "f16",  "topk",     150,  0.5),
+    ("batch16_threshold_bf16",   16, 2048, 1024, 8192,  "bf16", "threshold", 0,   0.5),
+    ("opt13b_neurons_b32_f16",   32, 5120, 1024, 20480, "f16",  "topk",     1024, 0.5),
+    ("opt30b_neurons_b24_bf16",  24, 7168, 1024, 28672, "bf16", "topk",     1434, 0.5),
 ]
 
 
@@ -105,6 +110,20 @@ def test_predict_two_predictors_fused():
     got = _run(y, [(PA1, PA2, "topk", 7, 0.5, 7), (PM1, PM2, "topk", 410, 0.5, 410)], "f16")
     _compare(y, PA1, PA2, "topk", 7, 0.5, got[0])
     _compare(y, PM1, PM2, "topk", 410, 0.5, got[1])
+
+
+def test_predict_two_predictors_fused_batched():
+    """Head and neuron predictors of one layer in one call for 20 rows (the
+    tensor-core path: one launch per product holds both predictors' tiles)."""
+    B, d = 20, 5120
+    y = draw((B, d), 1.0, 103, "y", "f16")
+    PA1 = draw((512, d), d ** -0.5, 103, "PA1", "f16")
+    PA2 = draw((40, 512), 512 ** -0.5, 103, "PA2", "f16")
+    PM1 = draw((1024, d), d ** -0.5, 103, "PM1", "f16")
+    PM2 = draw((20480, 1024), 1024 ** -0.5, 103, "PM2", "f16")
+    got = _run(y, [(PA1, PA2, "topk", 8, 0.5, 8), (PM1, PM2, "threshold", 0, 0.5, 20480)], "f16")
+    _compare(y, PA1, PA2, "topk", 8, 0.5, got[0])
+    _compare(y, PM1, PM2, "threshold", 0, 0.5, got[1])
 
 
 def test_threshold_capacity_truncates_and_reports():
