@@ -203,6 +203,21 @@ cudaError_t launch_sparse_attn(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
 cudaError_t launch_kv_repair(const AttnLaunch& a, dv_dtype dt, WsHeader* hdr,
                              cudaStream_t stream);
 
+// q/K/V of one token with the selected heads' KV repair on the tensor cores
+// (k_qkv_tc.cu): batch 1, 16-bit storage, d_h 128, d a multiple of 64, at
+// most 4096 cache positions.  Also appends the token (X[p], valid column p).
+struct Qkv1Launch {
+  const void* y; int d, h;
+  const void* Wqkv;
+  void* K; void* V; void* X; uint8_t* valid; int n_max;
+  const int32_t* pos;
+  const int32_t* U; const int32_t* U_count; int capU;  // the row's head list
+  float* q;                                            // [capU][128]
+  int pdl;                                             // launched with overlap
+};
+bool qkv1_tc_supported(int B, int d, int d_h, int n_max, dv_dtype dt);
+cudaError_t launch_qkv1_tc(const Qkv1Launch& a, dv_dtype dt, WsHeader* hdr, cudaStream_t stream);
+
 // Bulk K/V fill of the missing positions on the tensor cores (k_kv_tc.cu):
 // 16-bit storage, d_h 64 or 128.
 bool kv_tc_supported(int d, int d_h, dv_dtype dt);

@@ -1145,7 +1145,14 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
     a.repair_only = 1;
   }
   // single-pass rows of 3 chunks stage their vectors in dynamic shared memory
-  if (wide) {
+  if (!tc && qkv1_tc_supported(a.B, a.d, a.d_h, a.n_max, dtype_of<T>())) {
+    // batch 1: weight tiles on the tensor cores, repairs as extra columns
+    Qkv1Launch q{};
+    q.y = L.y; q.d = a.d; q.h = a.h; q.Wqkv = L.Wqkv;
+    q.K = L.K; q.V = L.V; q.X = L.X; q.valid = L.valid; q.n_max = a.n_max; q.pos = L.pos;
+    q.U = a.U; q.U_count = a.U_count; q.capU = a.capU; q.q = a.q; q.pdl = pdl;
+    e = launch_qkv1_tc(q, dtype_of<T>(), hdr, stream);
+  } else if (wide) {
     if (qc_wide <= 6)
       e = launch_k(attn_qkv_kernel<T, 6, 2>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
     else if (qc_wide <= 8)

@@ -254,6 +254,65 @@ def test_repair_beyond_one_scan_window():
         assert within_ulp_product(V[i, m], f64(Xp)[m], f64(Wqkv)[i, 2], "f16"), f"V head {i}"
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_repair_chunks_batch1_d128(dtype):
+    """Batch 1, d_h 128 (the tensor-core projection): heads with 0, 12, 13
+    and 75 skipped positions (the current token plus 12 skipped positions
+    fill the first 16-column chunk; 13 spill one into a second chunk, 75 take
+    five), planted stale values at the skipped positions, including position
+    0 and p - 1.  Every skipped row is recomputed within the product bound,
+    the valid flags end all set, and the output matches the oracle."""
+    B, d, h, d_h, n_max, P = 1, 1024, 5, 128, 2048, 1500
+    name = "chunks/" + dtype
+    torch_dt = TORCH[dtype]
+    Wqkv, Wo = _layer(name, d, h, d_h, dtype, None)
+    dev = "cuda"
+    Wqkv_d, Wo_d = Wqkv.to(dev), Wo.to(dev)
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch_dt, dev)
+    Xp = draw((P, d), 1.0, 311, name + "/X", dtype)
+    kv.X[0, :P].copy_(Xp.to(dev))
+    pos = torch.tensor([P], dtype=torch.int32, device=dev)
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, h, n_max))
+    dv.dv_kv_repair(kv, Wqkv_d, pos, torch.arange(h, dtype=torch.int32, device=dev)[None],
+                    torch.tensor([h], dtype=torch.int32, device=dev), ws)
+    assert dv.dv_check(ws)[0] == 0
+    g = torch.Generator().manual_seed(11)
+    misses = {0: torch.empty(0, dtype=torch.long),
+              1: torch.randperm(P, generator=g)[:12],
+              3: torch.cat([torch.randperm(P - 2, generator=g)[:11] + 1, torch.tensor([0, P - 1])]),
+              4: torch.cat([torch.randperm(P - 2, generator=g)[:73] + 1, torch.tensor([0, P - 1])])}
+    for i, mi in misses.items():
+        mi = torch.unique(mi)
+        misses[i] = mi
+        if mi.numel():
+            kv.valid[0, i, mi.to(dev)] = 0
+            kv.K[0, i, mi.to(dev)] = 7.0
+            kv.V[0, i, mi.to(dev)] = -7.0
+    assert [misses[i].numel() for i in (0, 1, 3, 4)] == [0, 12, 13, 75]
+    cache = oracle.KVCache.empty(h, n_max, d_h, d, dtype)
+    cache.X[:P] = f64(Xp)
+    cache.K[:, :P] = f64(kv.K)[0, :, :P]
+    cache.V[:, :P] = f64(kv.V)[0, :, :P]
+    cache.valid[:, :P] = kv.valid[0, :, :P].cpu().numpy() == 1
+    y = draw((B, d), 1.0, 311, name + "/y", dtype)
+    S = [0, 1, 3, 4]
+    out = torch.zeros(B, d, device=dev)
+    ws1 = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, len(S), n_max))
+    dv.dv_sparse_attn(y.to(dev), Wqkv_d, Wo_d, kv, pos, torch.tensor([S], dtype=torch.int32, device=dev),
+                      torch.tensor([len(S)], dtype=torch.int32, device=dev), 0.125, out, ws1)
+    assert dv.dv_check(ws1)[0] == 0
+    ref = oracle.sparse_attn(f64(y)[0], f64(Wqkv), f64(Wo), cache, P, S, 0.125)
+    assert_rel_l2(f64(out)[0], ref, dtype, "chunked repairs")
+    K, V, valid = f64(kv.K)[0], f64(kv.V)[0], kv.valid[0].cpu().numpy()
+    for i in S:
+        assert np.all(valid[i, : P + 1] == 1)
+        m = np.concatenate([misses[i].numpy(), [P]]).astype(np.int64)
+        Xm = np.concatenate([f64(Xp), f64(y)])[np.minimum(m, P)]
+        assert within_ulp_product(K[i, m], Xm, f64(Wqkv)[i, 1], dtype), f"K head {i}"
+        assert within_ulp_product(V[i, m], Xm, f64(Wqkv)[i, 2], dtype), f"V head {i}"
+    assert np.all(valid[2, :P] == 1) and valid[2, P] == 0  # unselected head: column P cleared
+
+
 def test_position_outside_cache_is_reported():
     B, d, h, d_h, n_max = 1, 128, 4, 64, 16
     Wqkv, Wo = _layer("pos", d, h, d_h, "f16", None)
