@@ -20,8 +20,11 @@
 // producer of y (launch overlap); the decode kernel marks the repaired
 // positions valid, as after the CUDA-core projection kernel.
 //
-// One thread issues the TMA copies into a 5-stage ring, one issues the MMAs;
-// every wait is bounded (dv_set_wait_limit_ns) and reports DV_ERR_TIMEOUT.
+// The first stages' weight tiles are requested right after set-up, before
+// the scan for skipped positions and before the wait for y.  One thread
+// issues the TMA copies into a 5-stage ring (two CTAs per SM), one issues the
+// MMAs; every wait is bounded (dv_set_wait_limit_ns) and
+// reports DV_ERR_TIMEOUT.
 // Block 0 also appends the token: X[p] = y and the valid column p.
 
 #include <cuda.h>
@@ -38,7 +41,6 @@ namespace {
 constexpr int kQM = 128;   // rows per tile = d_h
 constexpr int kQN = 16;    // MMA N: vectors per chunk
 constexpr int kQKB = 64;   // d elements per stage
-constexpr int kQSt = 5;
 constexpr int kQThreads = 128;
 constexpr int kQMaxPos = 4096;  // n_max bound: the skipped positions of a head fit one list
 constexpr long long kUnwindNs = 2000000000LL;
@@ -83,14 +85,14 @@ __device__ void append_token(const Qkv1Args& a, int p, int nU) {
   }
 }
 
-template <typename T>
+template <typename T, int ST>
 __global__ void __launch_bounds__(kQThreads, 1)
     qkv1_tc_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapY,
                    const __grid_constant__ CUtensorMap mapX, Qkv1Args a) {
   constexpr uint32_t kABytes = kQM * 128, kBBytes = kQN * 128;
   constexpr uint32_t kTmemCols = 32;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kQSt], empty[kQSt], done;
+  __shared__ uint64_t full[ST], empty[ST], done;
   __shared__ uint32_t tmem_base;
   __shared__ uint16_t miss_s[kQMaxPos];
   __shared__ int tmp[32];
@@ -127,6 +129,36 @@ __global__ void __launch_bounds__(kQThreads, 1)
     return;
   }
 
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + ST * kABytes;
+  float* red = reinterpret_cast<float*>(sB + ST * kBBytes);  // [128][17] partial tile (S > 1)
+  if (tid == 0) {
+    for (int q = 0; q < ST; ++q) {
+      tc::mbar_init(&full[q], 1);
+      tc::mbar_init(&empty[q], 1);
+    }
+    tc::mbar_init(&done, 1);
+    tc::fence_mbar_init();
+    issued = consumed = flag_err = 0;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base;
+  const int nk_all = (a.d + kQKB - 1) / kQKB;
+  const int kb0 = split * nk_all / S;
+  const int nk = (split + 1) * nk_all / S - kb0;  // >= 2: the host keeps nk_all >= 2 S
+  const int wrow = (i * 3 + m) * kQM;
+  // the first stages' weights now: nothing else is needed to request them
+  const int first = min(nk, ST);
+  if (tid == 0)
+    for (int kb = 0; kb < first; ++kb) {
+      tc::mbar_expect_tx(&full[kb], kABytes);
+      tc::tma_load_2d(sA + kb * kABytes, &mapW, (kb0 + kb) * kQKB, wrow, &full[kb]);
+    }
+
   // skipped positions j < p of head i (K and V tiles), ascending; p <= 4096,
   // each thread scans 32 flags
   int nmiss = 0;
@@ -151,31 +183,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if ((j0 + k < p) && (((w8[k >> 2] >> (8 * (k & 3))) & 0xffu) == 0)) miss_s[r++] = (uint16_t)(j0 + k);
     nmiss = total;
   }
+  __syncthreads();  // miss_s is complete
   // chunk 0 takes 12 skipped positions beside y, later chunks 16
   const int nch = 1 + (nmiss > 12 ? (nmiss - 12 + kQN - 1) / kQN : 0);
 
-  uint8_t* smem = align1024(smem_raw);
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kQSt * kABytes;
-  float* red = reinterpret_cast<float*>(sB + kQSt * kBBytes);  // [128][17] partial tile (S > 1)
-  if (tid == 0) {
-    for (int q = 0; q < kQSt; ++q) {
-      tc::mbar_init(&full[q], 1);
-      tc::mbar_init(&empty[q], 1);
-    }
-    tc::mbar_init(&done, 1);
-    tc::fence_mbar_init();
-    issued = consumed = flag_err = 0;
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_base;
-  const int nk_all = (a.d + kQKB - 1) / kQKB;
-  const int kb0 = split * nk_all / S;
-  const int nk = (split + 1) * nk_all / S - kb0;  // >= 1: the host keeps nk_all >= 4 S
-  const int wrow = (i * 3 + m) * kQM;
   bool waited = false;
 
   for (int ch = 0; ch < nch; ++ch) {
@@ -195,30 +206,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
       };
       int kb = 0;
       if (!waited) {
-        // the first stages' weights and stored inputs before the wait for y
-        const int first = min(nk, kQSt);
+        // chunk 0: the first stages' weights are in flight; their stored
+        // inputs now, y after the wait
         for (; kb < first; ++kb) {
-          const int g = ch * nk + kb, st = g % kQSt;
-          if (g >= kQSt && !tc::mbar_wait(&empty[st], ((g / kQSt) - 1) & 1, a.wait_ns)) {
-            set_error(a.hdr, DV_ERR_TIMEOUT, 41);
-            flag_err = 1;
-            break;
-          }
-          tc::mbar_arrive_expect_tx(&full[st], bytes);
-          tc::tma_load_2d(sA + st * kABytes, &mapW, (kb0 + kb) * kQKB, wrow, &full[st]);
-          issue_x(st, (kb0 + kb) * kQKB);
+          tc::mbar_arrive_expect_tx(&full[kb], bytes - kABytes);
+          issue_x(kb, (kb0 + kb) * kQKB);
         }
         if (a.pdl) grid_dep_wait();
         grid_dep_launch();  // the decode kernel may be scheduled
         waited = true;
-        for (int k2 = 0; k2 < kb; ++k2) {
-          const int st = (ch * nk + k2) % kQSt;
-          tc::tma_gather4(sB + st * kBBytes, &mapY, (kb0 + k2) * kQKB, 0, 0, 0, 0, &full[st]);
-        }
+        for (int k2 = 0; k2 < kb; ++k2)
+          tc::tma_gather4(sB + k2 * kBBytes, &mapY, (kb0 + k2) * kQKB, 0, 0, 0, 0, &full[k2]);
       }
       for (; kb < nk && !flag_err; ++kb) {
-        const int g = ch * nk + kb, st = g % kQSt;
-        if (g >= kQSt && !tc::mbar_wait(&empty[st], ((g / kQSt) - 1) & 1, a.wait_ns)) {
+        const int g = ch * nk + kb, st = g % ST;
+        if (g >= ST && !tc::mbar_wait(&empty[st], ((g / ST) - 1) & 1, a.wait_ns)) {
           set_error(a.hdr, DV_ERR_TIMEOUT, 42);
           flag_err = 1;
           break;
@@ -233,8 +235,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
       const uint32_t idesc = tc::idesc_f16(kQM, kQN, kBf16, false, false);
       for (int kb = 0; kb < nk && !flag_err; ++kb) {
-        const int g = ch * nk + kb, st = g % kQSt;
-        if (!tc::mbar_wait(&full[st], (g / kQSt) & 1, a.wait_ns)) {
+        const int g = ch * nk + kb, st = g % ST;
+        if (!tc::mbar_wait(&full[st], (g / ST) & 1, a.wait_ns)) {
           set_error(a.hdr, DV_ERR_TIMEOUT, 43);
           flag_err = 1;
           break;
@@ -296,9 +298,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int c = 0; c < kQN; ++c) red[tid * (kQN + 1) + c] = good ? v[c] : 0.f;
       cluster_arrive();
       cluster_wait();
-      const int span = kQM / S, r0 = split * span;
-      for (int e = tid; e < span * ncol; e += kQThreads) {
-        const int c = e / span, t = r0 + (e - c * span);
+      const int span = (kQM + S - 1) / S, r0 = split * span, nr = max(0, min(kQM - r0, span));
+      for (int e = tid; e < nr * ncol; e += kQThreads) {
+        const int c = e / nr, t = r0 + (e - c * nr);
         float z = 0.f;
         for (int q = 0; q < S; ++q) z += ld_dsmem_f32(red + t * (kQN + 1) + c, (uint32_t)q);
         if (good) store(t, c, z);
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // no TMA write into this CTA's shared memory may still be in flight
   if (tid == 0) {
     for (int g = consumed; g < issued; ++g)
-      if (!tc::mbar_wait(&full[g % kQSt], (g / kQSt) & 1, unwind_ns)) break;
+      if (!tc::mbar_wait(&full[g % ST], (g / ST) & 1, unwind_ns)) break;
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -321,12 +323,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
 }
 
-template <typename T>
+template <typename T, int ST>
 cudaError_t qkv1_attr(size_t smem) {
   static PerDevice attr;  // function attributes are per device
   return (cudaError_t)attr.get(current_device(), [smem] {
-    cudaError_t e = cudaFuncSetAttribute(qkv1_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return (int)e;
+    return (int)cudaFuncSetAttribute(qkv1_tc_kernel<T, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
 }
 
@@ -338,6 +339,16 @@ int sm_count() {
       n = 148;
     return n;
   });
+}
+
+template <typename T, int ST>
+cudaError_t qkv1_launch(CUtensorMap& mW, CUtensorMap& mY, CUtensorMap& mX, Qkv1Args& a, int tiles, int pdl,
+                        cudaStream_t stream) {
+  const size_t smem = 1024 + ST * (kQM * 128 + kQN * 128) + (size_t)kQM * (kQN + 1) * 4;
+  cudaError_t e = qkv1_attr<T, ST>(smem);
+  if (e != cudaSuccess) return e;
+  return launch_k(qkv1_tc_kernel<T, ST>, dim3(tiles * a.S), dim3(kQThreads), smem, stream, pdl != 0, a.S, mW, mY,
+                  mX, a);
 }
 
 template <typename T>
@@ -354,15 +365,15 @@ cudaError_t qkv1_t(const Qkv1Launch& L, WsHeader* hdr, cudaStream_t stream) {
   a.pdl = L.pdl; a.hdr = hdr; a.wait_ns = wait_limit_ns();
   const int tiles = 3 * L.capU;
   const int nk = (L.d + kQKB - 1) / kQKB;
-  // split d while two CTAs per SM still hold the grid and each split keeps
-  // 4+ stages of work
+  const int sms = sm_count();
+  // Split d into S slices (one cluster of S CTAs per tile), doubling S while
+  // two CTAs per SM still hold the grid and every slice keeps 4+ stages.
+  // Clusters of 5 or 6 CTAs (one wave on paper) measured slower: with the
+  // previous kernel still resident under launch overlap, whole clusters wait
+  // for room in a GPC, so the grid keeps slack.
   a.S = 1;
-  while (a.S < 8 && tiles * a.S * 2 <= 2 * sm_count() && nk >= 8 * a.S) a.S *= 2;
-  const size_t smem = 1024 + kQSt * (kQM * 128 + kQN * 128) + (size_t)kQM * (kQN + 1) * 4;
-  cudaError_t e = qkv1_attr<T>(smem);
-  if (e != cudaSuccess) return e;
-  return launch_k(qkv1_tc_kernel<T>, dim3(tiles * a.S), dim3(kQThreads), smem, stream, L.pdl != 0, a.S, mW, mY,
-                  mX, a);
+  while (a.S < 8 && tiles * a.S * 2 <= 2 * sms && nk >= 8 * a.S) a.S *= 2;
+  return qkv1_launch<T, 5>(mW, mY, mX, a, tiles, L.pdl, stream);
 }
 
 }  // namespace
