@@ -25,7 +25,8 @@
 // issues the TMA copies into a 5-stage ring (two CTAs per SM), one issues the
 // MMAs; every wait is bounded (dv_set_wait_limit_ns) and
 // reports DV_ERR_TIMEOUT.
-// Block 0 also appends the token: X[p] = y and the valid column p.
+// Two warps of block 0 also append the token (X[p] = y, the valid column p)
+// while its tiles stream.
 
 #include <cuda.h>
 
@@ -68,20 +69,20 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // X[p] = y; valid[.][p] = 1 for the selected heads, 0 for the others (the
-// column may hold flags of an earlier pass over the cache).  Nothing in this
-// call reads X[p] or the column p.
+// column may hold flags of an earlier pass over the cache), by `nt` threads
+// (t0 = this thread's index among them), without a block barrier.  Nothing
+// in this call reads X[p] or the column p.
 template <typename T>
-__device__ void append_token(const Qkv1Args& a, int p, int nU) {
-  const int tid = threadIdx.x;
+__device__ void append_token(const Qkv1Args& a, int p, int nU, int t0, int nt) {
+  grid_dep_wait();  // y comes from the kernel before this one
   const int C = a.d / 8;
   const uint4* src = static_cast<const uint4*>(a.y);
   uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(a.X) + (size_t)p * a.d);
-  for (int c = tid; c < C; c += kQThreads) dst[c] = ld_cached(src + c);
-  for (int i = tid; i < a.h; i += kQThreads) a.valid[(size_t)i * a.n_max + p] = 0;
-  __syncthreads();
-  for (int e = tid; e < nU; e += kQThreads) {
-    const int i = a.U[e];
-    if (i >= 0 && i < a.h) a.valid[(size_t)i * a.n_max + p] = 1;
+  for (int c = t0; c < C; c += nt) dst[c] = ld_cached(src + c);
+  for (int i = t0; i < a.h; i += nt) {
+    uint8_t sel = 0;
+    for (int e = 0; e < nU; ++e) sel |= (uint8_t)(a.U[e] == i);
+    a.valid[(size_t)i * a.n_max + p] = sel;
   }
 }
 
@@ -113,8 +114,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (p < 0) {
         if (tid == 0) set_error(a.hdr, DV_ERR_POSITION, p0);
       } else {
-        grid_dep_wait();
-        append_token<T>(a, p, nU);
+        append_token<T>(a, p, nU, tid, kQThreads);
       }
     }
     return;
@@ -122,10 +122,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int i = a.U[u];
   if (i < 0 || i >= a.h) {
     if (tid == 0 && split == 0 && m == 0) set_error(a.hdr, DV_ERR_INDEX_RANGE, i);
-    if (appender) {
-      grid_dep_wait();
-      append_token<T>(a, p, nU);
-    }
+    if (appender) append_token<T>(a, p, nU, tid, kQThreads);
     return;
   }
 
@@ -231,6 +228,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         issue_x(st, (kb0 + kb) * kQKB);
       }
       issued = ch * nk + kb;
+    } else if (appender && ch == 0 && warp >= 2) {  // idle until the epilogue: append the token
+      append_token<T>(a, p, nU, tid - 64, kQThreads - 64);
     } else if (warp == 1 && lane == 0) {  // MMA issuer (after an error: only the commit)
       constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
       const uint32_t idesc = tc::idesc_f16(kQM, kQN, kBf16, false, false);
@@ -317,10 +316,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
-  if (appender) {
-    grid_dep_wait();
-    append_token<T>(a, p, nU);
-  }
 }
 
 template <typename T, int ST>
