@@ -258,9 +258,10 @@ def _block_bytes(w, B, mean_n, uA, uM, sumA):
 KNAMES = {"mlp": "dv_sparse_mlp", "attn": "dv_sparse_attn", "predict": "dv_predict",
           "ln": "dv_layernorm"}
 KERNELS = {"mlp": "mlp_fused_kernel (batch 1; else union + up + combine, or union + tcgen05 up/down)",
-           "attn": "attn_qkv_kernel + attn_decode_kernel + rows_combine_kernel "
-                   "(8+ rows: repair plan + tcgen05 q/K/V + decode + tcgen05 output projection)",
-           "predict": "rows_dot x2 + select_kernel (8+ rows: pred_tc_kernel x2 + select_kernel)",
+           "attn": "batch 1: qkv1_tc_kernel (16-bit, d_h 128; else attn_qkv_kernel) + attn_decode_kernel + "
+                   "rows_combine_kernel or rows_stream_kernel; 2+ rows: repair plan + tcgen05 q/K/V + decode + "
+                   "tcgen05 output projection",
+           "predict": "rows_dot x2 + select_kernel (2+ rows: pred_tc_kernel x2 + select_kernel)",
            "ln": "layernorm_kernel"}
 
 
@@ -550,7 +551,7 @@ def _time_stack(args, dec, w, B, full_layers, world=1):
             e["gbs_in_step"] = per[k] / (ins * 1e-6) / 1e9
             e["frac_in_step"] = e["gbs_in_step"] / hbm
         blocks[k] = e
-    if B >= 8 and w.dtype != "f32":
+    if B >= 2 and w.dtype != "f32":
         # tensor-core MLP: the union contraction's flops (both products)
         fl = 4.0 * uM * w.d * B
         t = blocks["mlp"]["us_per_call_isolated"] * 1e-6

@@ -96,7 +96,7 @@ cudaError_t launch_predict(const void* y, int B, int d, dv_dtype dt,
                            const PredLaunch& p, int n_preds, WsHeader* hdr,
                            cudaStream_t stream);
 
-// Both products of the predictor for 8..32 rows on tcgen05 (k_predict_tc.cu):
+// Both products of the predictor for 2..32 rows on tcgen05 (k_predict_tc.cu):
 // scores into p.s; the selection is launched by launch_predict.
 bool predict_tc_supported(int B, int d, dv_dtype dt, const PredLaunch& p, int n_preds);
 cudaError_t launch_predict_tc(const void* y, int B, int d, dv_dtype dt, const PredLaunch& p, int n_preds,
@@ -124,8 +124,10 @@ struct MlpLaunch {
 // Room for the batch union of B lists of up to `cap` neurons out of N.
 int mlp_union_cap(int B, int N, int cap);
 
-// Batches of at least this many rows use the tcgen05 path (16-bit types).
-constexpr int kTcMinBatch = 8;
+// Batches of at least this many rows use the tcgen05 paths (16-bit types);
+// batch 1 has its own kernels.  Four rows on CUDA cores took 814 us per
+// OPT-30B-shaped layer at half the units kept, 339 us on the tensor cores.
+constexpr int kTcMinBatch = 2;
 bool tc_mlp_supported(int B, int d, dv_dtype dt);
 int tc_act_cols(int N);
 cudaError_t launch_sparse_mlp_tc(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
@@ -134,7 +136,7 @@ cudaError_t launch_sparse_mlp_tc(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
 cudaError_t launch_sparse_mlp(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
                               int num_sms, cudaStream_t stream);
 
-// Batched attention on the tensor cores (k_mlp_tc.cu; 8+ rows, 16-bit, d a
+// Batched attention on the tensor cores (k_mlp_tc.cu; 2+ rows, 16-bit, d a
 // multiple of 128).  Projections of the union heads' Wqkv rows (`rows`,
 // `rows_count` on the device, at most max_rows) with the current tokens: q
 // of the member rows in fp32, K/V at pos rounded into the cache.

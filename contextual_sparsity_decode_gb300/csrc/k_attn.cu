@@ -1133,7 +1133,7 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   // three chunks per thread when a row fits (fewer registers), else four
   const int pdl = (launch_overlap() > 0 && a.B == 1) ? 1 : 0;
   cudaError_t e;
-  // batches of 8+ rows in a 16-bit type: the projections of the current
+  // batches of 2+ rows in a 16-bit type: the projections of the current
   // tokens and the output projection are dense contractions over the union
   // of the rows' heads and run on the tensor cores; attn_qkv only repairs
   const bool tc = a.B > 1 && L.rows && tc_mlp_supported(a.B, a.d, dtype_of<T>());

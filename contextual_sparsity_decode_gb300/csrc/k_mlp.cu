@@ -14,7 +14,7 @@
 //                 writer per output element (rows_combine.cuh).
 // At batch 1 both run in one launch (mlp_fused_kernel) when its grid fits
 // on the GPU at once; otherwise as mlp_up_kernel + rows_combine_kernel.
-// Batches of 8+ rows in a 16-bit type use the tcgen05 path (k_mlp_tc.cu).
+// Batches of 2+ rows in a 16-bit type use the tcgen05 path (k_mlp_tc.cu).
 
 #include <cstdlib>
 

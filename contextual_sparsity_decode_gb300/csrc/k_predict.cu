@@ -5,7 +5,7 @@
 // Launch 1 (rows_dot<ReLU>):    h = ReLU(y P1)       both predictors
 // Launch 2 (rows_dot<Sigmoid>): s = sigmoid(h P2)    both predictors
 // Launch 3 (select_kernel):     index lists, one CTA per (predictor, row)
-// Batches of 8..32 rows in 16-bit types run launches 1 and 2 on the tensor
+// Batches of 2..32 rows in 16-bit types run launches 1 and 2 on the tensor
 // cores instead (k_predict_tc.cu).
 //
 // Both GEMVs are HBM-bound row streams.  A CTA owns a tile of rows; a group

@@ -1,4 +1,4 @@
-// The sparsity predictor for batches of 8+ rows on the tcgen05 tensor cores
+// The sparsity predictor for batches of 2..32 rows on the tcgen05 tensor cores
 // ("用Deja Vu来提高 LLM 的推理速度" §2: a two-layer MLP with a sigmoid per head /
 // neuron).  With B rows both products are dense contractions over the
 // predictor's weights, whose rows are contiguous:

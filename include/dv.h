@@ -206,7 +206,7 @@ dv_status dv_sparse_mlp_workspace_size(int B, int d, int N, int cap,
  * out [B][d] fp32: overwritten (accumulate = 0) or added to (accumulate = 1,
  * e.g. a residual stream).  Below 8 rows every output element has one
  * writer and a fixed summation order, so results repeat bit for bit; the
- * tensor-core path (8+ rows of a 16-bit type) adds partial sums with fp32
+ * tensor-core path (2+ rows of a 16-bit type) adds partial sums with fp32
  * atomics, so there the last bits of out may differ between runs.
  * Limits: B <= 32, d <= 16384 (8192 for DV_F32), N <= 65536. */
 dv_status dv_sparse_mlp(const void* y, int B, int d, int N,

@@ -69,7 +69,7 @@ def _run(y, W1n, W2n, sets, cap, accumulate=False, base=None):
 
 
 def _marks(case):
-    # batches of 8+ rows in a 16-bit type run on the tcgen05 path
+    # batches of 2+ rows in a 16-bit type run on the tcgen05 path
     return [pytest.mark.tc] if case[1] >= 8 and case[4] != "f32" else []
 
 

@@ -33,7 +33,7 @@ CASES = [
     ("kN_f16",                   1, 256,   64,   500,   "f16",  "topk",     500,  0.5),
     ("batch8_f16",               8, 1024,  256,  4096,  "f16",  "topk",     205,  0.5),
     ("batch32_bf16",             32, 1024, 256,  4096,  "bf16", "topk",     205,  0.5),
-    # tensor-core predictor (8..32 rows): ragged rows, r and d off the tiles
+    # tensor-core predictor (2..32 rows): ragged rows, r and d off the tiles
     ("batch13_ragged_f16",       13, 1032, 200,  3000,  "f16",  "topk",     150,  0.5),
     ("batch16_threshold_bf16",   16, 2048, 1024, 8192,  "bf16", "threshold", 0,   0.5),
     ("opt13b_neurons_b32_f16",   32, 5120, 1024, 20480, "f16",  "topk",     1024, 0.5),
