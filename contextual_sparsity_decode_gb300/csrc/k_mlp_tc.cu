@@ -5,13 +5,16 @@
 // (Deja Vu reading notes, "Sparsified MLP", applied to every row with the
 // row's own set as a mask):
 //   up    a[u][b] = ReLU(W^1[:, U[u]] . y_b) * [U[u] in S_b]
-//         M = 128 union neurons per CTA, N = B padded to 16/32, K = d.
+//         M = 128 union neurons per tile, N = B padded to 16/32, K = d,
+//         split over a cluster of S <= 8 CTAs when the union has few tiles
+//         (partials summed through distributed shared memory before ReLU).
 //         A = gathered rows of W1n (TMA gather4, 128-byte swizzle, K-major),
 //         B = y (TMA tile, K-major).  Accumulator in TMEM; the epilogue writes
 //         a split into two storage-type halves hi + lo (a = hi + lo to ~2^-17
 //         relative), so the second product keeps fp32-level accuracy.
 //   down  out[b][c] += sum_u W^2[c, U[u]] a[u][b]
-//         M = 128 output columns per CTA, N = B padded, K = a chunk of U.
+//         M = 128 output columns per CTA, N = B padded, K = a chunk of U
+//         (256..1024 entries, sized to fill the GPU).
 //         A = gathered rows of W2n read as an MN-major operand (a neuron row
 //         is 64 contiguous columns per 128-byte swizzle row), B = a_hi and
 //         a_lo (two MMAs per K step).  Split-K over U with fp32 atomics.
@@ -42,7 +45,7 @@ constexpr int kKB = 64;                  // K elements per stage (one 128-byte r
 // (measured on GB300: rings of 200 KB, one CTA per SM, were 1.3-1.5x slower).
 constexpr int kSU = 5;
 constexpr int kSD = 4;
-constexpr int kKChunk = 1024;            // union neurons per down-projection CTA
+constexpr int kKChunk = 1024;            // union neurons per down-projection CTA, at most
 constexpr long long kUnwindNs = 2000000000LL;  // two seconds
 constexpr uint32_t kTmemCols = 32;
 
@@ -66,6 +69,7 @@ struct UpArgs {
   float* q;                 // [B][capQ][d_h]
   void* K;
   void* V;
+  int S;                    // CTAs (one cluster) per tile, splitting K
 };
 
 // Epilogues of the up kernel: the MLP's masked ReLU split into two storage
@@ -81,6 +85,7 @@ struct DownArgs {
   WsHeader* hdr;
   long long wait_ns;
   int tile_rows;  // 1: every 64-row chunk of the row list is contiguous (two tile loads a stage)
+  int kchunk;     // union entries per CTA (grid y), a multiple of 64, <= kKChunk
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -141,8 +146,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
   const int cnt = max(0, min(*a.U_count, a.capU));
-  const int u0 = blockIdx.x * kTM;
-  if (u0 >= cnt) return;  // whole CTA, before any barrier or TMEM use
+  const int S = a.S;
+  const int tile = (int)blockIdx.x / S, split = (int)blockIdx.x % S;
+  const int u0 = tile * kTM;
+  if (u0 >= cnt) return;  // whole cluster, before any barrier or TMEM use
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
@@ -171,7 +178,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int nk = a.d / kKB;
+  const int nk_all = a.d / kKB;
+  const int kb0 = split * nk_all / S;  // this CTA's K blocks [kb0, kb0 + nk)
+  const int nk = (split + 1) * nk_all / S - kb0;
 
   if (warp >= 4) {
     if (warp == 4 && lane == 0) {  // TMA producer: y (and the weight rows when they form one tile)
@@ -183,10 +192,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc::mbar_arrive_expect_tx(&fullB[s], kBBytes);
-        tc::tma_load_2d(sB + s * kBBytes, &mapY, kb * kKB, 0, &fullB[s]);
+        tc::tma_load_2d(sB + s * kBBytes, &mapY, (kb0 + kb) * kKB, 0, &fullB[s]);
         if (a.tile_rows) {
           tc::mbar_arrive_expect_tx(&fullA[s], kABytes);
-          tc::tma_load_2d(sA + s * kABytes, &mapT, kb * kKB, rows[0], &fullA[s]);
+          tc::tma_load_2d(sA + s * kABytes, &mapT, (kb0 + kb) * kKB, rows[0], &fullA[s]);
         }
         issued = kb + 1;
       }
@@ -224,7 +233,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int r = (tid >> 3) + 16 * q;
-      src[q] = reinterpret_cast<const uint8_t*>(static_cast<const T*>(W) + (size_t)rows[r] * a.d + ch * 8);
+      src[q] = reinterpret_cast<const uint8_t*>(static_cast<const T*>(W) + (size_t)rows[r] * a.d +
+                                                (size_t)kb0 * kKB + ch * 8);
       off[q] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4));
     }
     if (!gather_rows_pipeline<kSU>(sA, kABytes, src, off, nk, kKB * sizeof(T), fullA, empty, a.wait_ns)) {
@@ -233,61 +243,81 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  // epilogue (warps 0-3): thread = accumulator row (union entry u0 + tid)
-  bool ok = true;
+  // epilogue: accumulator row = tile row (union entry u0 + row)
   float v[BP];
   if (tid < kTM) {
-    ok = tc::mbar_wait(&done, 0, unwind_ns);
-    if (!ok && lane == 0) set_error(a.hdr, DV_ERR_TIMEOUT, 3);
+    const bool ok = tc::mbar_wait(&done, 0, unwind_ns);
+    if (!ok && lane == 0) {
+      set_error(a.hdr, DV_ERR_TIMEOUT, 3);
+      flag_err = 1;
+    }
     __syncwarp();
     tc::fence_after_sync();
 #pragma unroll
     for (int c = 0; c < BP; c += 8) tc::tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16) + c, v + c);
     tc::tmem_ld_wait();
   }
-  __syncthreads();  // flag_err is final
-  if (tid < kTM) {
-    const int u = u0 + tid;
-    const bool live = ok && !flag_err && u < cnt;
-    const int row = rows[tid];
-    if (EPI == kEpiMlp) {
-      T* hi = static_cast<T*>(a.act_hi);
-      T* lo = static_cast<T*>(a.act_lo);
-#pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        float x = fmaxf(v[b], 0.f);
-        if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
-        const T h = Elem<T>::from_f(x);
-        const T l = Elem<T>::from_f(x - Elem<T>::to_f(h));
-        hi[(size_t)b * a.Upad + u] = h;
-        lo[(size_t)b * a.Upad + u] = l;
-      }
-    } else if (live) {
-      const int dh3 = 3 * a.d_h;
-      const int i = row / dh3, rem = row - i * dh3, m = rem / a.d_h, t = rem - m * a.d_h;
-      const int slot = m == 0 ? a.slot_of[i] : 0;
-      T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
-#pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        if (b >= a.B || !bit_test(a.member + (size_t)b * a.words, i)) continue;
-        if (m == 0) {
-          a.q[((size_t)b * a.capQ + slot) * a.d_h + t] = v[b];
-        } else {
-          const int p = a.pos[b];
-          if (p >= 0 && p < a.n_max) dst[(((size_t)b * a.h + i) * a.n_max + p) * a.d_h + t] = Elem<T>::from_f(v[b]);
-        }
-      }
-    }
-  }
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();  // flag_err is final
   // no TMA write into this CTA's shared memory may still be in flight (the
-  // loaders waited for their own copies)
+  // loaders waited for their own copies); after this the ring is free
   if (tid == 0) {
     for (int kb = consumed; kb < issued; ++kb) {
       if (!tc::mbar_wait(&fullB[kb % kSU], (kb / kSU) & 1, unwind_ns)) break;
       if (a.tile_rows && !tc::mbar_wait(&fullA[kb % kSU], (kb / kSU) & 1, unwind_ns)) break;
     }
+  }
+  __syncthreads();
+  const bool good = !flag_err;
+  // element (tile row tr, batch row b) of the finished accumulator
+  auto emit = [&](int tr, int b, float z) {
+    const int u = u0 + tr;
+    const bool live = good && u < cnt;
+    const int row = rows[tr];
+    if (EPI == kEpiMlp) {
+      float x = fmaxf(z, 0.f);
+      if (!live || b >= a.B || !bit_test(a.member + (size_t)b * a.words, row)) x = 0.f;
+      const T h = Elem<T>::from_f(x);
+      static_cast<T*>(a.act_hi)[(size_t)b * a.Upad + u] = h;
+      static_cast<T*>(a.act_lo)[(size_t)b * a.Upad + u] = Elem<T>::from_f(x - Elem<T>::to_f(h));
+    } else {
+      if (!live || b >= a.B) return;
+      const int dh3 = 3 * a.d_h;
+      const int i = row / dh3, rem = row - i * dh3, m = rem / a.d_h, t = rem - m * a.d_h;
+      if (!bit_test(a.member + (size_t)b * a.words, i)) return;
+      if (m == 0) {
+        a.q[((size_t)b * a.capQ + a.slot_of[i]) * a.d_h + t] = z;
+      } else {
+        const int p = a.pos[b];
+        T* dst = static_cast<T*>(m == 1 ? a.K : a.V);
+        if (p >= 0 && p < a.n_max) dst[(((size_t)b * a.h + i) * a.n_max + p) * a.d_h + t] = Elem<T>::from_f(z);
+      }
+    }
+  };
+  if (S == 1) {
+    if (tid < kTM) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b) emit(tid, b, v[b]);
+    }
+  } else {
+    // park the partial tile in the (now idle) ring, then sum rows
+    // [split * span, +span) over the cluster's partials
+    float* red = reinterpret_cast<float*>(sA);  // [128][BP + 1]
+    if (tid < kTM) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b) red[tid * (BP + 1) + b] = good ? v[b] : 0.f;
+    }
+    cluster_arrive();
+    cluster_wait();
+    const int span = (kTM + S - 1) / S, r0 = split * span, nr = max(0, min(kTM - r0, span));
+    for (int e = tid; e < nr * BP; e += kTcThreads) {
+      const int b = e / nr, tr = r0 + (e - b * nr);
+      float z = 0.f;
+      for (int q = 0; q < S; ++q) z += ld_dsmem_f32(red + tr * (BP + 1) + b, (uint32_t)q);
+      emit(tr, b, z);
+    }
+    cluster_arrive();  // no CTA leaves while another reads its partials
+    cluster_wait();
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -308,9 +338,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
   const int cnt = max(0, min(*a.U_count, a.capU));
   const int c0 = blockIdx.x * kTM;
-  const int k0 = blockIdx.y * kKChunk;
+  const int k0 = blockIdx.y * a.kchunk;
   if (k0 >= cnt) return;
-  const int k1 = min(cnt, k0 + kKChunk);
+  const int k1 = min(cnt, k0 + a.kchunk);
   const int nk = (k1 - k0 + kKB - 1) / kKB;
 
   uint8_t* smem = align1024(smem_raw);
@@ -443,7 +473,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();  // flag_err is final
   if (tid < kTM && ok && !flag_err) {
     const int col = c0 + tid;
-    for (int b = 0; b < a.B; ++b) atomicAdd(a.out + (size_t)b * a.d + col, v[b]);
+#pragma unroll
+    for (int b = 0; b < BP; ++b)
+      if (b < a.B) atomicAdd(a.out + (size_t)b * a.d + col, v[b]);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -458,6 +490,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ---- host ------------------------------------------------------------------------
+
+int sm_count() {
+  static PerDevice sms;
+  return sms.get(current_device(), [] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, current_device()) != cudaSuccess || n <= 0)
+      n = 148;
+    return n;
+  });
+}
+
+// CTAs per up-projection tile: double while two CTAs per SM still hold the
+// grid and every slice of d keeps 4+ stages (a small union otherwise leaves
+// most SMs idle: 23 tiles of 128 rows streamed 1.8 MB each).
+int up_splits(int tiles, int nk_all) {
+  int S = 1;
+  while (S < 8 && tiles * S * 2 <= 2 * sm_count() && nk_all >= 8 * S) S *= 2;
+  return S;
+}
+
+// Union entries per down-projection CTA: about two CTAs per SM over the
+// column tiles, 256..1024 entries.
+int down_chunk(int col_tiles, int max_rows) {
+  const int want = max(1, 2 * sm_count() / max(1, col_tiles));
+  int ch = (max_rows + want - 1) / want;
+  ch = (ch + kKB - 1) / kKB * kKB;
+  return max(4 * kKB, min(kKChunk, ch));
+}
 
 template <typename T, int BP>
 cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
@@ -482,15 +542,18 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   const int maxU = L.N < L.B * L.cap ? L.N : L.B * L.cap;
   UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr,
             wait_limit_ns()};
+  const int tiles = (maxU + kTM - 1) / kTM;
+  ua.S = up_splits(tiles, L.d / kKB);
   // neuron rows are gathered by the CTAs' own threads (mapT is not used)
-  mlp_tc_up_kernel<T, BP><<<(maxU + kTM - 1) / kTM, kTcThreads, smem_up, stream>>>(mY, mY, L.W1n, ua);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_k(mlp_tc_up_kernel<T, BP, kEpiMlp>, dim3(tiles * ua.S), dim3(kTcThreads), smem_up, stream,
+                           false, ua.S, mY, mY, L.W1n, ua);
   if (e != cudaSuccess) return e;
   DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr, wait_limit_ns()};
-  dim3 g(L.d / kTM, (maxU + kKChunk - 1) / kKChunk);
+  da.kchunk = down_chunk(L.d / kTM, maxU);
+  dim3 g(L.d / kTM, (maxU + da.kchunk - 1) / da.kchunk);
   mlp_tc_down_kernel<T, BP><<<g, kTcThreads, smem_dn, stream>>>(mHi, mLo, mHi, L.W2n, da);
   e = cudaGetLastError();
-  if (e == cudaSuccess) count_launches(2);
+  if (e == cudaSuccess) count_launches(1);
   return e;
 }
 
@@ -516,11 +579,10 @@ cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream)
   // a head's 3 d_h rows are contiguous: with d_h = 128 every 128-row tile is
   // one head's Q, K or V block
   ua.tile_rows = (3 * L.d_h) % kTM == 0 ? 1 : 0;
-  mlp_tc_up_kernel<T, BP, kEpiQkv><<<(L.max_rows + kTM - 1) / kTM, kTcThreads, smem_up, stream>>>(mY, mT, L.Wqkv,
-                                                                                                   ua);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) count_launches(1);
-  return e;
+  const int tiles = (L.max_rows + kTM - 1) / kTM;
+  ua.S = up_splits(tiles, L.d / kKB);
+  return launch_k(mlp_tc_up_kernel<T, BP, kEpiQkv>, dim3(tiles * ua.S), dim3(kTcThreads), smem_up, stream, false,
+                  ua.S, mY, mT, L.Wqkv, ua);
 }
 
 template <typename T, int BP>
@@ -539,7 +601,8 @@ cudaError_t run_rows_tc(const TcRowsLaunch& L, WsHeader* hdr, cudaStream_t strea
   if (ea != cudaSuccess) return ea;
   DownArgs da{L.rows, L.rows_count, L.n_rows, L.B, L.d, L.n_rows, L.out, hdr, wait_limit_ns(),
               L.rows_per_unit % kKB == 0 ? 1 : 0};
-  dim3 g(L.d / kTM, (L.max_rows + kKChunk - 1) / kKChunk);
+  da.kchunk = down_chunk(L.d / kTM, L.max_rows);
+  dim3 g(L.d / kTM, (L.max_rows + da.kchunk - 1) / da.kchunk);
   mlp_tc_down_kernel<T, BP><<<g, kTcThreads, smem_dn, stream>>>(mHi, mLo, mT, L.W, da);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(1);
