@@ -66,6 +66,9 @@ def _args(argv=None):
     p.add_argument("--cpu-layers", type=int, default=2,
                    help="layers of the workload in the oracle's timed sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--prefill", choices=("synthetic", "dense"), default="synthetic",
+                   help="prompt state: drawn layer inputs with their K/V (fast), or the dense "
+                        "causal prompt pass through every layer (timed and reported)")
     return p.parse_args(argv)
 
 
@@ -317,10 +320,27 @@ def run_stack(args, w, B, rank, world, local, full_layers, with_e2e=True):
     scale = 1.0 / math.sqrt(w.d_h)
     n_cache = (w.n_max + 15) // 16 * 16  # the cache holds a multiple of 16 positions
     dec = SparseDecoder(layers, B, n_cache, w.k_heads, w.k_neurons, scale)
-    dec.prefill([torch.stack([embeddings(w, w.n_prompt, f"X{l}" if B == 1 else f"X{l}/{b}", device=dev)
-                              for b in range(B)]) for l in range(w.layers)], w.n_prompt)
+    prefill = None
+    if getattr(args, "prefill", "synthetic") == "dense":
+        # the prompt through every layer with all heads and neurons, position
+        # by position (the decode kernels with S = all)
+        E = torch.stack([embeddings(w, w.n_prompt, f"E/{b}", device=dev).float() for b in range(B)])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dec.prefill_dense(E, w.n_prompt)
+        torch.cuda.synchronize()
+        dt_s = time.perf_counter() - t0
+        prefill = {"kind": "dense causal prompt pass, S = all heads and neurons, one graph per position",
+                   "positions": w.n_prompt, "layers": w.layers, "rows": B, "s": dt_s,
+                   "positions_per_s": w.n_prompt * B / dt_s}
+        del E
+    else:
+        dec.prefill([torch.stack([embeddings(w, w.n_prompt, f"X{l}" if B == 1 else f"X{l}/{b}", device=dev)
+                                  for b in range(B)]) for l in range(w.layers)], w.n_prompt)
     dec.r_stream.copy_(residual_input(w, B, "r0", device=dev))
     out = _time_stack(args, dec, w, B, full_layers, world)
+    if prefill is not None:
+        out["prefill"] = prefill
     tokens = args.steps * B * world
     if with_e2e:
         # ---- end to end through the public API with host buffers

@@ -124,6 +124,73 @@ class SparseDecoder:
         if st != 0:
             raise dv.DvError(st, "prefill", f"info={info}")
 
+    def _dense_ops(self):
+        """One prompt position through every layer with all heads and all
+        neurons selected (no predictor), on the current stream."""
+        if self.trace:
+            self.r_in0.copy_(self.r_stream)
+        for l in range(self.L):
+            W = self.layers[l]
+            dv.dv_layernorm(self.r_stream, self.y_a[l], self.eps)
+            dv.dv_sparse_attn(self.y_a[l], W["Wqkv"], W["Wo"], self.kv[l], self.pos,
+                              self.head_idx[l], self.head_cnt[l], self.scale, self.r_stream,
+                              self.ws_attn, accumulate=True)
+            if self.trace:
+                self.r_mid[l].copy_(self.r_stream)
+            dv.dv_layernorm(self.r_stream, self.y_m[l], self.eps)
+            dv.dv_sparse_mlp(self.y_m[l], W["W1n"], W["W2n"], self.neur_idx[l], self.neur_cnt[l],
+                             self.r_stream, self.ws_mlp, accumulate=True)
+            if self.trace:
+                self.r_out[l].copy_(self.r_stream)
+
+    def prefill_dense(self, E: torch.Tensor, n_prompt: int, on_position=None):
+        """Dense causal prompt pass (Deja Vu reading notes, "Typical LLM
+        procedure": the prompt runs through every layer, which builds each
+        layer's KV cache; generation then goes token by token).  Positions
+        0..n_prompt-1 in order, each through every layer with all heads and
+        all neurons selected -- the decode step's own kernels with S = all,
+        one CUDA graph replayed per position -- so position t attends over
+        positions 0..t (causal attention) and every layer's X, K, V and valid
+        flags below n_prompt are the model's own.  E [B][n_prompt][d] (fp32)
+        is the residual stream entering layer 0.  Afterwards the decoder
+        continues at n_prompt with its keep counts.  ``on_position(t)`` runs
+        after position t (the tests read the traced activations there)."""
+        keep = (self.k_heads, self.k_neurons)
+        dev, B = self.device, self.B
+        if n_prompt > self.n_max:
+            raise ValueError("prompt longer than the cache")
+        self.set_keep(self.h, self.N)
+        heads = torch.arange(self.h, dtype=torch.int32, device=dev).repeat(B, 1)
+        neurons = torch.arange(self.N, dtype=torch.int32, device=dev).repeat(B, 1)
+        for l in range(self.L):
+            self.kv[l].valid.zero_()
+            self.head_idx[l].copy_(heads)
+            self.head_cnt[l].fill_(self.h)
+            self.neur_idx[l].copy_(neurons)
+            self.neur_cnt[l].fill_(self.N)
+        self.pos.zero_()
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        # every attention / MLP call follows the layernorm that produces its
+        # input and no predictor runs: launch overlap holds for all of them
+        prev = dv.dv_set_launch_overlap(1)
+        try:
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(graph, stream=s):
+                    self._dense_ops()
+                    dv.dv_positions_advance(self.pos, 0, self.n_max)
+        finally:
+            dv.dv_set_launch_overlap(prev)
+        torch.cuda.current_stream().wait_stream(s)
+        for t in range(n_prompt):
+            self.r_stream.copy_(E[:, t])
+            graph.replay()
+            if on_position is not None:
+                on_position(t)
+        self.check()
+        self.set_keep(*keep)
+
     def _time(self, kind: str, stream=None):
         """Record a timing event (kept in self.t_ev) when timing ``kind``.
         Events are 'external' so that they are real event records inside a

@@ -66,6 +66,7 @@ from .core import (  # noqa: F401
     decode_layer,
     lookahead,
     decode_stack,
+    prefill_dense,
     neuron_norms,
     head_outputs_causal,
     head_norms,

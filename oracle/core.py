@@ -319,6 +319,28 @@ def decode_stack(r: np.ndarray, layers: List[dict], caches: List[KVCache],
     return r, sets
 
 
+def prefill_dense(E: np.ndarray, layers: List[dict], caches: List[KVCache],
+                  c: float, dtype: str) -> np.ndarray:
+    """The prompt phase ([notes] "Typical LLM procedure": the prompt is run
+    through every layer, which builds each layer's KV cache; generation then
+    goes token by token): the dense model, S_A = all heads and S_M = all
+    neurons, over prompt positions 0..T-1 in order.  Position t attends over
+    positions 0..t of its layer, which is causal attention; every layer
+    stores its attention input X[t] and the K/V of every head at t.
+
+    E [T][d] holds the residual stream entering layer 0 at each position.
+    Mutates ``caches``; returns the residual stream after the last layer,
+    [T][d]."""
+    E = np.asarray(E, dtype=np.float64)
+    h = layers[0]["Wqkv"].shape[0]
+    N = layers[0]["W1n"].shape[0]
+    every = [(np.arange(h), np.arange(N))] * len(layers)
+    out = np.zeros_like(E)
+    for t in range(E.shape[0]):
+        out[t], _ = decode_stack(E[t], layers, caches, t, c, dtype, h, N, force_sets=every)
+    return out
+
+
 # --------------------------------------------------------------------------
 # true-sparsity labels  ([blog] §1 Contextual Sparsity: run the sequence
 # through the layer, keep the heads and MLP neurons whose outputs have the

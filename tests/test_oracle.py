@@ -556,6 +556,40 @@ def test_stack_lookahead_composition():
     assert np.array_equal(out, r)
 
 
+def check_prefill_dense_equals_causal_textbook():
+    """The dense prompt pass (every head and neuron, positions in order,
+    token by token) equals a textbook causal pre-LN stack in matrix form over
+    the whole prompt: torch layer_norm, causal scaled-dot-product attention
+    (torch SDPA, is_causal), linear layers; every layer's stored inputs and
+    K/V rows are the matrix form's."""
+    L, T, c = 2, 6, 0.5
+    layers = _tiny_layers(L)
+    h, _, d_h, d = layers[0]["Wqkv"].shape
+    E = RNG(43).standard_normal((T, d))
+    caches = [core.KVCache.empty(h, T, d_h, d, "f64") for _ in range(L)]
+    out = core.prefill_dense(E, layers, caches, c, "f64")
+    ln = lambda v: F.layer_norm(v, (d,), eps=core.EPS_LN)
+    R = _t(E)
+    for l, W in enumerate(layers):
+        Y = ln(R)
+        Wq, Wk, Wv = (_t(W["Wqkv"][:, m]) for m in range(3))  # [h][d_h][d]
+        Q = torch.einsum("td,hed->hte", Y, Wq)
+        K = torch.einsum("td,hed->hte", Y, Wk)
+        V = torch.einsum("td,hed->hte", Y, Wv)
+        H = F.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=c)  # [h][T][d_h]
+        R = R + torch.einsum("hte,hed->td", H, _t(W["Wo"]))
+        R = R + F.linear(F.relu(F.linear(ln(R), _t(W["W1n"]))), _t(W["W2n"]).T)
+        assert np.allclose(caches[l].X[:T], Y.numpy(), rtol=1e-12, atol=1e-12)
+        assert np.allclose(caches[l].K[:, :T], K.numpy(), rtol=1e-12, atol=1e-12)
+        assert np.allclose(caches[l].V[:, :T], V.numpy(), rtol=1e-12, atol=1e-12)
+        assert caches[l].valid[:, :T].all()
+    assert np.allclose(out, R.numpy(), rtol=1e-11, atol=1e-11)
+
+
+def test_prefill_dense_equals_causal_textbook():
+    check_prefill_dense_equals_causal_textbook()
+
+
 # ---------------------------------------------------------------------------
 # planted mistakes: each plausible error in one oracle step fails some pin
 # ---------------------------------------------------------------------------
@@ -617,7 +651,8 @@ MUTANTS = [
     ("sigmoid", _sigmoid_sign_flipped, [check_predictor_golden, check_predictor_loops]),
     ("head_output", _head_output_no_normalise, [check_attn_golden, check_attn_all_equals_textbook_dense]),
     ("head_output", _head_output_drops_current, [check_attn_golden,
-                                                 check_attn_all_equals_textbook_dense]),
+                                                 check_attn_all_equals_textbook_dense,
+                                                 check_prefill_dense_equals_causal_textbook]),
     ("select_topk", _topk_ties_high_index, [check_predictor_golden, check_topk_brute_force,
                                             check_predictor_special_cases]),
     ("kv_repair", _repair_skipped, [check_attn_golden, check_attn_history_invariance]),

@@ -172,3 +172,73 @@ def test_opt13b_stack_all_layers_teacher_forced():
     1024-position prompt, for 8 decoded tokens: the benchmark's configuration."""
     w = WORKLOADS["opt13b_stack_fp16"]
     _teacher_forced(w, B=1, steps=8)
+
+
+def _prefill_teacher_forced(w: Workload, B: int):
+    """The dense prompt pass (SparseDecoder.prefill_dense) against the
+    oracle, position by position and layer by layer on the GPU's own inputs
+    (Deja Vu reading notes, "Typical LLM procedure"): LN outputs within one
+    ulp, the attention block with every head over the position's causal
+    prefix and the MLP with every neuron within rel-L2 1e-3, and after the
+    prompt every layer's stored inputs X, valid flags and K/V rows."""
+    dev = "cuda"
+    layers = [layer_weights(w, l, device=dev) for l in range(w.layers)]
+    n_max = ((w.n_prompt + 15) // 16) * 16
+    scale = 1.0 / math.sqrt(w.d_h)
+    dec = SparseDecoder(layers, B, n_max, w.k_heads, w.k_neurons, scale, trace=True)
+    E = torch.stack([embeddings(w, w.n_prompt, f"E/{b}", device=dev).float() for b in range(B)])
+    L = w.layers
+    recs = []
+
+    def record(t):
+        recs.append({"r_in0": _np(dec.r_in0), "r_mid": [_np(dec.r_mid[l]) for l in range(L)],
+                     "r_out": [_np(dec.r_out[l]) for l in range(L)],
+                     "y_a": [_np(dec.y_a[l]) for l in range(L)], "y_m": [_np(dec.y_m[l]) for l in range(L)]})
+
+    dec.prefill_dense(E, w.n_prompt, on_position=record)
+    assert dec.k_heads == w.k_heads and dec.k_neurons == w.k_neurons
+    assert dec.pos.cpu().tolist() == [w.n_prompt] * B
+    dt = w.dtype
+    E64 = _np(E)
+    every_h, every_n = list(range(w.h)), np.arange(w.N)
+    for l in range(L):
+        W = {k: v.detach().to("cpu", torch.float32).numpy() for k, v in dec.layers[l].items()}
+        caches = [oracle.KVCache.empty(w.h, n_max, w.d_h, w.d, dt) for _ in range(B)]
+        for t, rec in enumerate(recs):
+            r_in = rec["r_in0"] if l == 0 else rec["r_out"][l - 1]
+            if l == 0:
+                assert np.array_equal(r_in, E64[:, t]), f"position {t}: layer 0 input"
+            for b in range(B):
+                where = f"layer {l} position {t} row {b}"
+                assert within_ulp(rec["y_a"][l][b], oracle.layernorm(r_in[b]), dt), where + " LN_a"
+                assert within_ulp(rec["y_m"][l][b], oracle.layernorm(rec["r_mid"][l][b]), dt), \
+                    where + " LN_m"
+                ref_a = oracle.sparse_attn(rec["y_a"][l][b], W["Wqkv"], W["Wo"], caches[b], t, every_h, scale)
+                assert_rel_l2(rec["r_mid"][l][b] - r_in[b], ref_a, dt, where + " attention")
+                ref_m = oracle.sparse_mlp(rec["y_m"][l][b], W["W1n"], W["W2n"], every_n)
+                assert_rel_l2(rec["r_out"][l][b] - rec["r_mid"][l][b], ref_m, dt, where + " mlp")
+        kv = dec.kv[l]
+        T = w.n_prompt
+        for b in range(B):
+            assert np.array_equal(_np(kv.X[b])[:T], caches[b].X[:T]), f"layer {l} row {b} X"
+            valid = kv.valid[b].cpu().numpy().astype(bool)
+            assert valid[:, :T].all() and not valid[:, T:].any(), f"layer {l} row {b} valid flags"
+            for name, ref in (("K", caches[b].K), ("V", caches[b].V)):
+                got = _np(getattr(kv, name)[b])[:, :T]
+                acc = 4.0 * np.sqrt(w.d) * 2.0 ** -24 * np.abs(ref[:, :T]).max()
+                assert within_ulp(got, ref[:, :T], dt, acc_floor=acc), f"layer {l} row {b} {name}"
+
+
+def test_prefill_dense_two_rows_f16():
+    """Two sequences (the batched tensor-core paths with every unit)."""
+    w = Workload("prefill_b2", 35, d=256, h=4, d_h=64, N=512, r=64, dtype="f16", layers=2,
+                 n_prompt=9, n_gen=1, head_pct=50, neuron_pct=10)
+    _prefill_teacher_forced(w, B=2)
+
+
+def test_prefill_dense_one_row_bf16_dh128():
+    """One sequence, d_h = 128 (the batch-1 tensor-core projection with
+    every head: 4 tiles x 3 and the KV append at each position)."""
+    w = Workload("prefill_b1", 36, d=512, h=4, d_h=128, N=1024, r=64, dtype="bf16", layers=2,
+                 n_prompt=12, n_gen=1, head_pct=50, neuron_pct=10)
+    _prefill_teacher_forced(w, B=1)
