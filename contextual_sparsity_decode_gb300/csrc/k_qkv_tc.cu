@@ -12,9 +12,10 @@
 //             row) and up to 12 skipped positions' stored inputs X[j];
 //   chunk c:  16 further skipped positions (heads skipped for long).
 // Q tiles have only y.  Each tile is split along d over a cluster of S <= 8
-// CTAs; every CTA accumulates its slice of d in TMEM, parks the partial
-// 128 x 16 tile in shared memory, and after a cluster barrier sums 128 / S of
-// its rows over the S partials (distributed shared memory) and writes them:
+// CTAs; every CTA accumulates its slice of d in TMEM, pushes each partial
+// row into the shared memory of the CTA that owns the row (128 / S rows each,
+// distributed shared memory), and after one cluster barrier every CTA sums
+// its own rows over the S partials and writes them:
 // q in fp32, K/V rounded to the storage type at p and at the repaired
 // positions.  The weight tiles are requested before the wait for the
 // producer of y (launch overlap); the decode kernel marks the repaired
@@ -136,7 +137,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + ST * kABytes;
-  float* red = reinterpret_cast<float*>(sB + ST * kBBytes);  // [128][17] partial tile (S > 1)
+  float* red = reinterpret_cast<float*>(sB + ST * kBBytes);  // [S][span][17] pushed partials (S > 1)
   if (tid == 0) {
     for (int q = 0; q < ST; ++q) {
       tc::mbar_init(&full[q], 1);
@@ -299,19 +300,31 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int c = 0; c < kQN; ++c)
         if (good && c < ncol) store(tid, c, v[c]);
     } else {
+      // push this CTA's partial rows into the CTA that owns them (slot
+      // `split` of the owner's [S][span] rows), one cluster barrier, then
+      // sum the owned rows from local shared memory: no remote reads, so
+      // nothing waits for a second barrier before a CTA leaves
+      const int span = (kQM + S - 1) / S;
+      if (ch > 0) {  // the owners have finished the previous chunk's sums
+        cluster_arrive();
+        cluster_wait();
+      }
+      {
+        const int owner = tid / span, lr = tid - owner * span;
+        float* dst = red + ((size_t)split * span + lr) * (kQN + 1);
 #pragma unroll
-      for (int c = 0; c < kQN; ++c) red[tid * (kQN + 1) + c] = good ? v[c] : 0.f;
+        for (int c = 0; c < kQN; ++c)
+          if (c < ncol) st_dsmem_f32(dst + c, (uint32_t)owner, good ? v[c] : 0.f);
+      }
       cluster_arrive();
       cluster_wait();
-      const int span = (kQM + S - 1) / S, r0 = split * span, nr = max(0, min(kQM - r0, span));
+      const int r0 = split * span, nr = max(0, min(kQM - r0, span));
       for (int e = tid; e < nr * ncol; e += kQThreads) {
-        const int c = e / nr, t = r0 + (e - c * nr);
+        const int c = e / nr, lr = e - c * nr;
         float z = 0.f;
-        for (int q = 0; q < S; ++q) z += ld_dsmem_f32(red + t * (kQN + 1) + c, (uint32_t)q);
-        if (good) store(t, c, z);
+        for (int q = 0; q < S; ++q) z += red[((size_t)q * span + lr) * (kQN + 1) + c];
+        if (good) store(r0 + lr, c, z);
       }
-      cluster_arrive();  // no CTA reuses or leaves its partials while another reads them
-      cluster_wait();
     }
   }
 
@@ -345,7 +358,7 @@ int sm_count() {
 template <typename T, int ST>
 cudaError_t qkv1_launch(CUtensorMap& mW, CUtensorMap& mY, CUtensorMap& mX, Qkv1Args& a, int tiles, int pdl,
                         cudaStream_t stream) {
-  const size_t smem = 1024 + ST * (kQM * 128 + kQN * 128) + (size_t)kQM * (kQN + 1) * 4;
+  const size_t smem = 1024 + ST * (kQM * 128 + kQN * 128) + (size_t)(kQM + 8) * (kQN + 1) * 4;
   cudaError_t e = qkv1_attr<T, ST>(smem);
   if (e != cudaSuccess) return e;
   return launch_k(qkv1_tc_kernel<T, ST>, dim3(tiles * a.S), dim3(kQThreads), smem, stream, pdl != 0, a.S, mW, mY,
