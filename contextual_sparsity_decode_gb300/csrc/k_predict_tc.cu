@@ -11,9 +11,10 @@
 // Both predictors run in one launch per product (their CTAs side by side).
 // The first product has only r / 128 tiles per predictor (8 for r = 1024), so
 // each tile is split along d over a cluster of S <= 8 CTAs: every CTA
-// accumulates its slice of d in TMEM, parks the partial tile in shared memory,
-// and after a cluster barrier sums 128 / S of the tile's rows over the S
-// CTAs' partials (distributed shared memory) before ReLU and the split.
+// accumulates its slice of d in TMEM and pushes each partial row into the
+// shared memory of the CTA that owns the row (128 / S rows each, distributed
+// shared memory); after one cluster barrier every CTA sums its own rows over
+// the S partials before ReLU and the split.
 // On CUDA cores a batch of 32 read each predictor's weights once per 8-row
 // tile (4x) and was bound by fp32 FMA throughput.
 //
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kPSt * kABytes;  // [stage][kNB] tiles of BP rows
-  float* red = reinterpret_cast<float*>(sB + kPSt * kNB * kBBytes);  // [128][BP + 1] partial tile (S > 1)
+  float* red = reinterpret_cast<float*>(sB + kPSt * kNB * kBBytes);  // [S][128 / S][BP + 1] pushed partials (S > 1)
   if (tid == 0) {
     for (int q = 0; q < kPSt; ++q) {
       tc::mbar_init(&full[q], 1);
@@ -171,17 +172,23 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     } else {
-      // park the partial tile (a CTA without K blocks holds zeros), then sum
-      // rows [split * 128 / S, (split + 1) * 128 / S) over the cluster
+      // push the partial rows (zeros from a CTA without K blocks) into the
+      // CTA that owns them (slot `split` of its [S][span] rows), one cluster
+      // barrier, then sum the owned rows from local shared memory
+      const int span = kPM / a.S;
+      {
+        const int owner = tid / span, lr = tid - owner * span;
+        float* dst = red + ((size_t)split * span + lr) * (BP + 1);
 #pragma unroll
-      for (int b = 0; b < BP; ++b) red[tid * (BP + 1) + b] = (good && nk > 0) ? v[b] : 0.f;
+        for (int b = 0; b < BP; ++b) st_dsmem_f32(dst + b, (uint32_t)owner, (good && nk > 0) ? v[b] : 0.f);
+      }
       cluster_arrive();
       cluster_wait();
-      const int span = kPM / a.S, r0 = split * span;
+      const int r0 = split * span;
       for (int e = tid; e < span * BP; e += 128) {
-        const int rr = r0 + e / BP, b = e % BP;
+        const int b = e / span, lr = e - b * span, rr = r0 + lr;  // consecutive threads: consecutive rows
         float x = 0.f;
-        for (int q = 0; q < a.S; ++q) x += ld_dsmem_f32(red + rr * (BP + 1) + b, (uint32_t)q);
+        for (int q = 0; q < a.S; ++q) x += red[((size_t)q * span + lr) * (BP + 1) + b];
         if (good && m0 + rr < rows) {
           x = fmaxf(x, 0.f);
           const T h = Elem<T>::from_f(x);
@@ -189,8 +196,6 @@ __global__ void __launch_bounds__(128, 1)
           lo[(size_t)b * ld + m0 + rr] = Elem<T>::from_f(x - Elem<T>::to_f(h));
         }
       }
-      cluster_arrive();  // no CTA leaves while another reads its partials
-      cluster_wait();
     }
   } else if (good && m0 + tid < rows) {
     float* s = p ? a.s[1] : a.s[0];
