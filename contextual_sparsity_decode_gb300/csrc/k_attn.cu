@@ -775,7 +775,8 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
   float qr[E];
   const float* qg = a.q + ((size_t)b * a.capU + u) * DH + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; ++e) qr[e] = qg[e] * a.scale;
+  for (int e = 0; e < E; ++e) qr[e] = qg[e];  // the scale goes on the logits: no use of q
+                                               // before the K/V loads below are issued
 
   float mw = -INFINITY, lw = 0.f, acc[E];
 #pragma unroll
@@ -805,7 +806,7 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
           float dot = 0.f;
 #pragma unroll
           for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
-          lg[s2] = warp_sum(dot);
+          lg[s2] = warp_sum(dot) * a.scale;
           mb = fmaxf(mb, lg[s2]);
         }
       }
@@ -851,11 +852,13 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
     st_dsmem_f32(&cm[rank], 0u, M);
     st_dsmem_f32(&cl[rank], 0u, Lsum);
   }
-  // every position before p of a selected head is now present (repaired by attn_qkv)
-  uint8_t* vrow = a.valid + ((size_t)b * a.h + i) * a.n_max;
-  for (int j = j_lo + tid; j < min(j_hi, p); j += kDecThreads) vrow[j] = 1;
   cluster_arrive();
   cluster_wait();
+  // every position before p of a selected head is now present (repaired by
+  // attn_qkv); marked after the barrier, whose release would otherwise wait
+  // for these stores (only the next call reads the flags)
+  uint8_t* vrow = a.valid + ((size_t)b * a.h + i) * a.n_max;
+  for (int j = j_lo + tid; j < min(j_hi, p); j += kDecThreads) vrow[j] = 1;
   if (rank != 0) return;
   float Mg = -INFINITY;
   for (int r = 0; r < CSd; ++r) Mg = fmaxf(Mg, cm[r]);
