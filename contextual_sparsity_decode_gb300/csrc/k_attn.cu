@@ -698,6 +698,52 @@ template <> struct KvRaw<__nv_bfloat16, 2> : KvRaw16x2<__nv_bfloat16> {};
 // before the first use, online max/sum across batches), and pushes its
 // (max, sum, numerator[d_h]) into rank 0's shared memory; after one cluster
 // barrier rank 0 combines the CSd partials in rank order and writes H.
+// Butterfly sums of NV values per lane over the warp (NV a power of two,
+// 2 <= NV <= 16): at the step with lane bit m (16, 8, ...) each lane keeps
+// the half of its values that its bit selects and adds the partner's copy of
+// that half.  Afterwards lane l holds the full sum of value butterfly_pos(l);
+// every value's sum sits in 32 / NV lanes.
+template <int NV>
+__device__ __forceinline__ float butterfly_sums(float (&v)[NV], int lane) {
+  int n = NV;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    if (n > 1) {
+      const bool up = (lane & m) != 0;
+      const int h = n >> 1;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < h) {
+          const float send = up ? v[i] : v[i + h];
+          const float keep = up ? v[i + h] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+    }
+  }
+  return v[0];
+}
+// The value index a lane holds after butterfly_sums<NV> (bits taken from the
+// lane's high bits, one per halving step), and the first lane holding value j.
+template <int NV>
+__device__ __forceinline__ int butterfly_pos(int lane) {
+  int j = 0, n = NV;
+#pragma unroll
+  for (int m = 16; m >= 1 && n > 1; m >>= 1, n >>= 1) j = 2 * j + ((lane & m) ? 1 : 0);
+  return j;
+}
+template <int NV>
+__device__ __forceinline__ int butterfly_lane(int j) {
+  int lane = 0, n = NV, m = 16;
+#pragma unroll
+  for (int b = NV >> 1; b >= 1; b >>= 1, m >>= 1) lane |= (j & b) ? m : 0;
+  (void)n;
+  return lane;
+}
+
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxCSd = 16;  // CTAs per decode cluster, at most
@@ -795,20 +841,29 @@ __global__ void __launch_bounds__(kDecThreads) attn_decode_kernel(AttnArgs a) {
           vraw[s2] = KvRaw<T, E>::load(Vr + (size_t)j * DH);
         }
       }
+      // the batch's kPB logits: per-lane partial dots, then one butterfly
+      // over the warp that halves the values each lane keeps at every step
+      // (kPB - 1 shuffles for the sums instead of kPB x 5) and leaves the sum
+      // for position bfly_pos(lane) in lanes 2i and 2i + 1; a broadcast per
+      // position gives every lane all of them
       float lg[kPB];
-      float mb = -INFINITY;
 #pragma unroll
       for (int s2 = 0; s2 < kPB; ++s2) {
-        lg[s2] = -INFINITY;
+        lg[s2] = 0.f;
         if (jb + s2 < jw1) {
           float kf[E];
           KvRaw<T, E>::to_f(kraw[s2], kf);
-          float dot = 0.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) dot = fmaf(qr[e], kf[e], dot);
-          lg[s2] = warp_sum(dot) * a.scale;
-          mb = fmaxf(mb, lg[s2]);
+          for (int e = 0; e < E; ++e) lg[s2] = fmaf(qr[e], kf[e], lg[s2]);
         }
+      }
+      const float mine = butterfly_sums<kPB>(lg, lane) * a.scale;
+      float mb = -INFINITY;
+#pragma unroll
+      for (int s2 = 0; s2 < kPB; ++s2) {
+        const float v = __shfl_sync(0xffffffffu, mine, butterfly_lane<kPB>(s2));
+        lg[s2] = jb + s2 < jw1 ? v : -INFINITY;
+        mb = fmaxf(mb, lg[s2]);
       }
       const float mn = fmaxf(mw, mb);
       const float corr = expf(mw - mn);  // 0 on the first batch (mw = -inf)
