@@ -46,6 +46,7 @@ CASES = [
     ("wide_f16_20k",     1, 20480, 2, 64,  "f16",  [20],          32,   3,    1,     "isq",  0.02),
     # selected W^O rows >= 48 MB at batch 1: the output projection streams them
     ("stream_wo_f16",    1, 12288, 24, 128, "f16", [40],          64,   3,    16,    "isq",  0.02),
+    ("stream_wo_f32",    1, 8192,  32, 64,  "f32", [20],          48,   2,    24,    "isq",  0.02),
     # 2+ rows of a 16-bit type: projections and output projection on the tensor cores,
     # repairs of skipped heads planned per (row, head)
     ("batch16_f16_tc",   16, 512, 8,  64,  "f16",  [20 + b for b in range(16)], 64, 6, 3, "isq", None),
