@@ -24,17 +24,6 @@ dv_status cuda_fail(cudaError_t e) {
 
 namespace {
 
-int num_sms_current() {
-  static PerDevice cache;
-  const int dev = current_device();
-  return cache.get(dev, [dev] {
-    int n = 0;
-    if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    return n;
-  });
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 

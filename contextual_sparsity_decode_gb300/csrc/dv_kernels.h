@@ -67,6 +67,9 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return e;
 }
 
+// SM count of the current device (cached per device).
+int num_sms_current();
+
 // Launch policy (dv_set_launch_overlap): 1 lets the first kernel of a batch-1
 // attention or MLP call start during the kernel before the call (k_misc.cu).
 int launch_overlap();

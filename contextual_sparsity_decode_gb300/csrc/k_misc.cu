@@ -141,4 +141,15 @@ cudaError_t launch_positions_advance(int32_t* pos, int B, int lo, int hi, cudaSt
   return e;
 }
 
+int num_sms_current() {
+  static PerDevice cache;  // SM counts are per device
+  const int dev = current_device();
+  return cache.get(dev, [dev] {
+    int n = 0;
+    if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    return n;
+  });
+}
+
 }  // namespace dv

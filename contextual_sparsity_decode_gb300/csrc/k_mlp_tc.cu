@@ -491,29 +491,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---- host ------------------------------------------------------------------------
 
-int sm_count() {
-  static PerDevice sms;
-  return sms.get(current_device(), [] {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, current_device()) != cudaSuccess || n <= 0)
-      n = 148;
-    return n;
-  });
-}
-
 // CTAs per up-projection tile: double while two CTAs per SM still hold the
 // grid and every slice of d keeps 4+ stages (a small union otherwise leaves
 // most SMs idle: 23 tiles of 128 rows streamed 1.8 MB each).
 int up_splits(int tiles, int nk_all) {
   int S = 1;
-  while (S < 8 && tiles * S * 2 <= 2 * sm_count() && nk_all >= 8 * S) S *= 2;
+  while (S < 8 && tiles * S * 2 <= 2 * num_sms_current() && nk_all >= 8 * S) S *= 2;
   return S;
 }
 
 // Union entries per down-projection CTA: about two CTAs per SM over the
 // column tiles, 256..1024 entries.
 int down_chunk(int col_tiles, int max_rows) {
-  const int want = max(1, 2 * sm_count() / max(1, col_tiles));
+  const int want = max(1, 2 * num_sms_current() / max(1, col_tiles));
   int ch = (max_rows + want - 1) / want;
   ch = (ch + kKB - 1) / kKB * kKB;
   return max(4 * kKB, min(kKChunk, ch));

@@ -224,16 +224,6 @@ cudaError_t pred_attr(size_t smem) {
   });
 }
 
-int sm_count() {
-  static PerDevice sms;
-  return sms.get(current_device(), [] {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, current_device()) != cudaSuccess || n <= 0)
-      n = 148;
-    return n;
-  });
-}
-
 template <typename T, int BP>
 cudaError_t pred_tc_t(const void* y, int B, int d, const PredLaunch& P, int n_preds, WsHeader* hdr,
                       cudaStream_t stream) {
@@ -253,7 +243,7 @@ cudaError_t pred_tc_t(const void* y, int B, int d, const PredLaunch& P, int n_pr
   const int tiles = a.tiles0 + (n_preds > 1 ? (P.r[1] + kPM - 1) / kPM : 0);
   const int nk = (d + kPKB - 1) / kPKB;
   a.S = 1;  // split d while the grid is below the SM count and each split keeps 2+ K blocks
-  while (a.S < 8 && tiles * a.S < sm_count() && nk >= 4 * a.S) a.S *= 2;
+  while (a.S < 8 && tiles * a.S < num_sms_current() && nk >= 4 * a.S) a.S *= 2;
   const size_t smem1 = 1024 + kPSt * (kPM * 128 + BP * 128) + (size_t)kPM * (BP + 1) * 4;
   cudaError_t e = pred_attr<T, BP, false>(smem1);
   if (e != cudaSuccess) return e;

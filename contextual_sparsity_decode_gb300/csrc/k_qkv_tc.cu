@@ -345,16 +345,6 @@ cudaError_t qkv1_attr(size_t smem) {
   });
 }
 
-int sm_count() {
-  static PerDevice sms;
-  return sms.get(current_device(), [] {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, current_device()) != cudaSuccess || n <= 0)
-      n = 148;
-    return n;
-  });
-}
-
 template <typename T, int ST>
 cudaError_t qkv1_launch(CUtensorMap& mW, CUtensorMap& mY, CUtensorMap& mX, Qkv1Args& a, int tiles, int pdl,
                         cudaStream_t stream) {
@@ -379,7 +369,7 @@ cudaError_t qkv1_t(const Qkv1Launch& L, WsHeader* hdr, cudaStream_t stream) {
   a.pdl = L.pdl; a.hdr = hdr; a.wait_ns = wait_limit_ns();
   const int tiles = 3 * L.capU;
   const int nk = (L.d + kQKB - 1) / kQKB;
-  const int sms = sm_count();
+  const int sms = num_sms_current();
   // Split d into S slices (one cluster of S CTAs per tile), doubling S while
   // two CTAs per SM still hold the grid and every slice keeps 4+ stages.
   // Clusters of 5 or 6 CTAs (one wave on paper) measured slower: with the
