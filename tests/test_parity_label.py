@@ -91,15 +91,21 @@ def test_head_norms(case):
     _labels(norms, ref, k, name)
 
 
-def test_select_scores_topk_threshold_and_ties():
+@pytest.mark.parametrize("N", [5000, 20000, 20001])
+def test_select_scores_topk_threshold_and_ties(N):
     """Rows of non-negative scores with repeated values: top-k (ties to the
-    lower index) and threshold lists equal the oracle's exactly."""
+    lower index) and threshold lists equal the oracle's exactly.  With few
+    distinct values the cut's bin holds hundreds of keys, so the selection
+    refines to one key value and takes the lowest indices equal to it."""
     dev = "cuda"
     g = torch.Generator().manual_seed(5)
-    N = 5000
-    S = (torch.randint(0, 700, (3, N), generator=g).float() / 64.0)  # many ties
+    S_many = torch.randint(0, 700, (3, N), generator=g).float() / 64.0  # many ties
+    S_few = torch.randint(0, 16, (3, N), generator=g).float() / 8.0     # hundreds of keys per value
     ws = dv.workspace(256)
-    for mode, k, t in ((dv.DV_TOPK, 400, 0.0), (dv.DV_TOPK, 1, 0.0), (dv.DV_THRESHOLD, 0, 9.5)):
+    for S, mode, k, t in ((S_many, dv.DV_TOPK, 400, 0.0), (S_many, dv.DV_TOPK, 1, 0.0),
+                          (S_many, dv.DV_TOPK, N - 1, 0.0), (S_many, dv.DV_TOPK, 4000, 0.0),
+                          (S_many, dv.DV_THRESHOLD, 0, 9.5), (S_few, dv.DV_TOPK, 777, 0.0),
+                          (S_few, dv.DV_TOPK, N // 2, 0.0), (S_few, dv.DV_THRESHOLD, 0, 1.0)):
         cap = N
         idx = torch.full((3, cap), -1, dtype=torch.int32, device=dev)
         cnt = torch.zeros(3, dtype=torch.int32, device=dev)
