@@ -314,6 +314,50 @@ def test_repair_chunks_batch1_d128(dtype):
     assert np.all(valid[2, :P] == 1) and valid[2, P] == 0  # unselected head: column P cleared
 
 
+def test_repair_every_position_at_the_cache_limit():
+    """Batch 1, d_h 128, a 4096-position cache (the largest the tensor-core
+    projection takes) at position 4000: one selected head has no valid K/V
+    at all (4000 skipped positions, ~250 chunks of stored inputs beside the
+    weight tiles), another is complete.  Every row is recomputed within the
+    product bound and the output matches the oracle."""
+    B, d, h, d_h, n_max, P = 1, 256, 3, 128, 4096, 4000
+    name = "limit"
+    Wqkv, Wo = _layer(name, d, h, d_h, "f16", None)
+    dev = "cuda"
+    Wqkv_d, Wo_d = Wqkv.to(dev), Wo.to(dev)
+    kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
+    Xp = draw((P, d), 1.0, 312, name + "/X", "f16")
+    kv.X[0, :P].copy_(Xp.to(dev))
+    ws = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, h, n_max))
+    # head 1 complete, heads 0 and 2 never computed
+    dv.dv_kv_repair(kv, Wqkv_d, torch.tensor([P], dtype=torch.int32, device=dev),
+                    torch.tensor([[1]], dtype=torch.int32, device=dev), torch.tensor([1], dtype=torch.int32, device=dev), ws)
+    assert dv.dv_check(ws)[0] == 0
+    kv.K[0, 0].fill_(7.0)
+    kv.V[0, 0].fill_(-7.0)
+    cache = oracle.KVCache.empty(h, n_max, d_h, d, "f16")
+    cache.X[:P] = f64(Xp)
+    cache.K[:, :P] = f64(kv.K)[0, :, :P]
+    cache.V[:, :P] = f64(kv.V)[0, :, :P]
+    cache.valid[:, :P] = kv.valid[0, :, :P].cpu().numpy() == 1
+    assert not cache.valid[0, :P].any() and cache.valid[1, :P].all()
+    y = draw((B, d), 1.0, 312, name + "/y", "f16")
+    S = [0, 1]
+    out = torch.zeros(B, d, device=dev)
+    ws1 = dv.workspace(dv.dv_sparse_attn_workspace_size(B, d, h, d_h, 2, n_max))
+    dv.dv_sparse_attn(y.to(dev), Wqkv_d, Wo_d, kv, torch.tensor([P], dtype=torch.int32, device=dev),
+                      torch.tensor([S], dtype=torch.int32, device=dev), torch.tensor([2], dtype=torch.int32, device=dev),
+                      1.0 / math.sqrt(d_h), out, ws1)
+    assert dv.dv_check(ws1)[0] == 0
+    ref = oracle.sparse_attn(f64(y)[0], f64(Wqkv), f64(Wo), cache, P, S, 1.0 / math.sqrt(d_h))
+    assert_rel_l2(f64(out)[0], ref, "f16", "position 4000")
+    K, V, valid = f64(kv.K)[0], f64(kv.V)[0], kv.valid[0].cpu().numpy()
+    Xall = np.concatenate([f64(Xp), f64(y)])
+    assert np.all(valid[0, : P + 1] == 1) and np.all(valid[1, : P + 1] == 1) and valid[2, P] == 0
+    assert within_ulp_product(K[0, : P + 1], Xall, f64(Wqkv)[0, 1], "f16"), "K head 0"
+    assert within_ulp_product(V[0, : P + 1], Xall, f64(Wqkv)[0, 2], "f16"), "V head 0"
+
+
 def test_position_outside_cache_is_reported():
     B, d, h, d_h, n_max = 1, 128, 4, 64, 16
     Wqkv, Wo = _layer("pos", d, h, d_h, "f16", None)
