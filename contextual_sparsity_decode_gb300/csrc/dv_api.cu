@@ -5,9 +5,25 @@
 #include <cstdint>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dv_kernels.h"
 
 using namespace dv;
+
+namespace {
+
+// A named NVTX range around each public call that enqueues work: profilers
+// that collect NVTX (ncu --nvtx, nsys) see the library's calls by name;
+// without one attached the push and pop are near no-ops.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
+}  // namespace
 
 namespace {
 
@@ -277,6 +293,7 @@ dv_status dv_predict_workspace_size(int B, int n_preds, int r_max, int N_max, si
 
 dv_status dv_predict(const void* y, int B, int d, dv_dtype dt, const dv_predictor* preds,
                      int n_preds, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  Range nvtx_range("dv_predict");
   dv_status st = check_pred(y, B, d, dt, preds, n_preds);
   if (st != DV_OK) return st;
   int r[2] = {0, 0}, N[2] = {0, 0};
@@ -304,6 +321,7 @@ dv_status dv_predict(const void* y, int B, int d, dv_dtype dt, const dv_predicto
 dv_status dv_lookahead(const void* y, int B, int d, dv_dtype dt, const dv_predictor* preds,
                        int n_preds, void* ws, size_t ws_bytes, cudaEvent_t input_ready,
                        cudaStream_t side, cudaEvent_t done) {
+  Range nvtx_range("dv_lookahead");
   dv_status st = check_pred(y, B, d, dt, preds, n_preds);
   if (st != DV_OK) return st;
   if (input_ready) {
@@ -333,6 +351,7 @@ dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, con
                         const int32_t* idx, int cap, const int32_t* count, dv_dtype dt,
                         float* out, int accumulate, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
+  Range nvtx_range("dv_sparse_mlp");
   if (!dtype_ok(dt)) return DV_ERR_DTYPE;
   if (!y || !W1n || !W2n || !idx || !count || !out) return DV_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(W1n) || !aligned16(W2n) || !aligned16(out) ||
@@ -372,6 +391,7 @@ dv_status dv_sparse_attn(const void* y, int B, int d, int h, int d_h, const void
                          const int32_t* head_idx, int cap, const int32_t* head_count, float scale,
                          dv_dtype dt, float* out, int accumulate, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
+  Range nvtx_range("dv_sparse_attn");
   dv_status st = check_attn(y, B, d, h, d_h, Wqkv, Wo, kv, pos, head_idx, cap, head_count, dt, true);
   if (st != DV_OK) return st;
   if (!out || !aligned16(out)) return DV_ERR_INVALID_ARG;
@@ -390,6 +410,7 @@ dv_status dv_kv_repair(const dv_kv* kv, int B, int d, int h, int d_h, const void
                        const int32_t* pos, const int32_t* head_idx, int cap,
                        const int32_t* head_count, dv_dtype dt, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
+  Range nvtx_range("dv_kv_repair");
   dv_status st = check_attn(nullptr, B, d, h, d_h, Wqkv, nullptr, kv, pos, head_idx, cap, head_count,
                             dt, false);
   if (st != DV_OK) return st;
@@ -427,6 +448,7 @@ dv_status check_label(const void* X, int T, int d, dv_dtype dt, const float* nor
 
 dv_status dv_label_neurons(const void* X, int T, int d, int N, const void* W1n, dv_dtype dt, float* norms,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
+  Range nvtx_range("dv_label_neurons");
   dv_status st = check_label(X, T, d, dt, norms, ws);
   if (st != DV_OK) return st;
   if (!W1n || !aligned16(W1n) || N < 1) return DV_ERR_INVALID_ARG;
@@ -443,6 +465,7 @@ dv_status dv_label_neurons(const void* X, int T, int d, int N, const void* W1n, 
 
 dv_status dv_label_heads(const void* X, int T, int d, int h, int d_h, const void* Wqkv, float scale,
                          dv_dtype dt, float* norms, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  Range nvtx_range("dv_label_heads");
   dv_status st = check_label(X, T, d, dt, norms, ws);
   if (st != DV_OK) return st;
   if (!Wqkv || !aligned16(Wqkv) || h < 1 || h > 1024) return DV_ERR_INVALID_ARG;
@@ -461,6 +484,7 @@ dv_status dv_label_heads(const void* X, int T, int d, int h, int d_h, const void
 
 dv_status dv_select_scores(const float* scores, int B, int N, dv_select mode, int k, float t, int32_t* idx, int cap,
                     int32_t* count, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  Range nvtx_range("dv_select_scores");
   if (!scores || !idx || !count || !aligned4(scores) || !aligned4(idx) || !aligned4(count))
     return DV_ERR_INVALID_ARG;
   if (B < 1 || B > 65535 || N < 1 || N > kSelectMaxN || cap < 1) return DV_ERR_INVALID_ARG;
@@ -475,6 +499,7 @@ dv_status dv_select_scores(const float* scores, int B, int N, dv_select mode, in
 
 dv_status dv_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtype dt,
                        cudaStream_t stream) {
+  Range nvtx_range("dv_layernorm");
   if (!dtype_ok(dt)) return DV_ERR_DTYPE;
   if (!x || !y || B < 1 || d < 4 || d > 16384 || d % 4 || !(eps >= 0.f)) return DV_ERR_INVALID_ARG;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 7u)) return DV_ERR_INVALID_ARG;
@@ -483,6 +508,7 @@ dv_status dv_layernorm(const float* x, int B, int d, float eps, void* y, dv_dtyp
 }
 
 dv_status dv_positions_advance(int32_t* pos, int B, int lo, int hi, cudaStream_t stream) {
+  Range nvtx_range("dv_positions_advance");
   if (!pos || B < 1 || lo < 0 || hi <= lo) return DV_ERR_INVALID_ARG;
   cudaError_t e = launch_positions_advance(pos, B, lo, hi, stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);
