@@ -164,10 +164,12 @@ def test_accumulate_into_residual():
 
 
 @pytest.mark.parametrize("accumulate", [False, True])
-def test_no_selected_head(accumulate):
+@pytest.mark.parametrize("d_h", [64, 128])
+def test_no_selected_head(accumulate, d_h):
     """An empty head set: MHA = 0, so out becomes 0 (or keeps the residual),
-    and the cache still records the token (X[pos], valid = 0)."""
-    B, d, h, d_h, n_max = 1, 512, 8, 64, 32
+    and the cache still records the token (X[pos], valid = 0).  d_h 128 takes
+    the batch-1 tensor-core projection, whose block 0 appends the token."""
+    B, d, h, n_max = 1, 512, 8, 32
     Wqkv, Wo = _layer("nohead", d, h, d_h, "f16", None)
     dev = "cuda"
     kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
@@ -358,8 +360,9 @@ def test_repair_every_position_at_the_cache_limit():
     assert within_ulp_product(V[0, : P + 1], Xall, f64(Wqkv)[0, 2], "f16"), "V head 0"
 
 
-def test_position_outside_cache_is_reported():
-    B, d, h, d_h, n_max = 1, 128, 4, 64, 16
+@pytest.mark.parametrize("d_h", [64, 128])
+def test_position_outside_cache_is_reported(d_h):
+    B, d, h, n_max = 1, 128, 4, 16
     Wqkv, Wo = _layer("pos", d, h, d_h, "f16", None)
     dev = "cuda"
     kv = dv.KV.empty(B, h, n_max, d_h, d, torch.float16, dev)
