@@ -264,17 +264,29 @@ class SparseDecoder:
             if self.trace:
                 self.r_out[l].copy_(self.r_stream)
 
-    def capture(self, advance: Optional[tuple] = None):
+    def capture(self, advance: Optional[tuple] = None, host_io: Optional[tuple] = None):
         """Capture one token (optionally followed by pos advance (lo, hi))
-        into a CUDA graph."""
+        into a CUDA graph.  host_io = (h_in, h_out), pinned host tensors of
+        the residual's shape: the graph then starts with the copy of h_in
+        into the residual stream and ends with the copy of the result into
+        h_out, so a host-driven loop costs one graph launch per token."""
         self.graph = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream())
+        if host_io is not None:
+            for t in host_io:
+                if t.device.type != "cpu" or not t.is_pinned() or t.shape != self.r_stream.shape \
+                        or t.dtype != self.r_stream.dtype:
+                    raise ValueError("host_io: pinned host fp32 tensors of the residual's shape")
         with torch.cuda.stream(s):
             with torch.cuda.graph(self.graph, stream=s):
+                if host_io is not None:
+                    self.r_stream.copy_(host_io[0], non_blocking=True)
                 self.step_ops()
                 if advance is not None:
                     dv.dv_positions_advance(self.pos, advance[0], advance[1])
+                if host_io is not None:
+                    host_io[1].copy_(self.r_stream, non_blocking=True)
         torch.cuda.current_stream().wait_stream(s)
 
     def replay(self):

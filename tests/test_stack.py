@@ -242,3 +242,45 @@ def test_prefill_dense_one_row_bf16_dh128():
     w = Workload("prefill_b1", 36, d=512, h=4, d_h=128, N=1024, r=64, dtype="bf16", layers=2,
                  n_prompt=12, n_gen=1, head_pct=50, neuron_pct=10)
     _prefill_teacher_forced(w, B=1)
+
+
+def test_host_io_graph_matches_device_loop():
+    """A host-driven token loop on a graph that carries its own copies
+    (capture(host_io=...): pinned input -> residual, step, residual -> pinned
+    output) gives bit for bit the tokens of the device-resident loop (batch 1:
+    every output element has one writer and a fixed summation order)."""
+    w = Workload("hostio_stack", 37, d=512, h=8, d_h=128, N=2048, r=128, dtype="f16", layers=3,
+                 n_prompt=30, n_gen=5, head_pct=25, neuron_pct=5)
+    dev = "cuda"
+    layers = [layer_weights(w, l, device=dev) for l in range(w.layers)]
+    n_max = ((w.n_prompt + 8 + 15) // 16) * 16
+    scale = 1.0 / math.sqrt(w.d_h)
+    Xp = [embeddings(w, w.n_prompt, f"X{l}", device=dev)[None] for l in range(w.layers)]
+    r0 = residual_input(w, 1, "r0", device=dev)
+    outs = []
+    for host in (False, True):
+        dec = SparseDecoder(layers, 1, n_max, w.k_heads, w.k_neurons, scale)
+        dec.prefill(Xp, w.n_prompt)
+        dec.r_stream.copy_(r0)
+        dec.step_ops()  # layer 0's first token eagerly, as in the stack tests
+        dv.dv_positions_advance(dec.pos, 0, n_max)
+        seq = []
+        if host:
+            h_in = torch.empty((1, w.d), dtype=torch.float32, pin_memory=True)
+            h_out = torch.empty((1, w.d), dtype=torch.float32, pin_memory=True)
+            h_in.copy_(dec.r_stream.cpu())
+            dec.capture(advance=(0, n_max), host_io=(h_in, h_out))
+            for _ in range(4):
+                dec.replay()
+                torch.cuda.current_stream().synchronize()
+                seq.append(h_out.clone())
+                h_in.copy_(h_out)
+        else:
+            dec.capture(advance=(0, n_max))
+            for _ in range(4):
+                dec.replay()
+                seq.append(dec.r_stream.cpu())
+        dec.check()
+        outs.append(seq)
+    for t, (a, b) in enumerate(zip(*outs)):
+        assert torch.equal(a, b), f"token {t}"
