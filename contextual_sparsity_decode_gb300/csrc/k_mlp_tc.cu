@@ -119,8 +119,8 @@ __device__ __forceinline__ bool gather_rows_pipeline(uint8_t* sA, uint32_t stage
 #pragma unroll
     for (int q = 0; q < 8; ++q) cp_async16(base + dst_off[q], src[q] + (size_t)kb * src_step);
     cp_async_commit();
-    if (kb >= S - 1) {
-      cp_async_wait<S - 1>();
+    if (kb >= S - 2) {
+      cp_async_wait<S - 2>();
       tc::fence_proxy_async();
       tc::mbar_arrive(&fullA[sig % S]);
       ++sig;
@@ -443,8 +443,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cp_async16(base + half * (kKB * 128) + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4), src);
       }
       cp_async_commit();
-      if (kb >= kSD - 1) {
-        cp_async_wait<kSD - 1>();
+      if (kb >= kSD - 2) {
+        cp_async_wait<kSD - 2>();
         tc::fence_proxy_async();
         tc::mbar_arrive(&fullA[sig % kSD]);
         ++sig;
