@@ -94,6 +94,8 @@ struct MlpWs {
   uint16_t* act_lo;
   float* act;
   int32_t* ctr;
+  float* tc_part;
+  int32_t* tc_sem;
 };
 MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   MlpWs w{};
@@ -106,6 +108,9 @@ MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   if (B >= kTcMinBatch) {
     w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(N));
     w.act_lo = c.take<uint16_t>((size_t)32 * tc_act_cols(N));
+    const int maxU = mlp_union_cap(B, N, cap);
+    w.tc_part = c.take<float>(tc_part_floats(maxU));
+    w.tc_sem = c.take<int32_t>((size_t)tc_act_cols(maxU) / 128);
   }
   return w;
 }
@@ -123,6 +128,8 @@ struct AttnWs {
   uint8_t* miss;
   uint16_t* act_hi;
   uint16_t* act_lo;
+  float* tc_part;
+  int32_t* tc_sem;
 };
 AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
   AttnWs w{};
@@ -140,6 +147,8 @@ AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
     w.miss = c.take<uint8_t>((size_t)B * h);
     w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(h * d_h));
     w.act_lo = c.take<uint16_t>((size_t)32 * tc_act_cols(h * d_h));
+    w.tc_part = c.take<float>(tc_part_floats(h * 3 * d_h));
+    w.tc_sem = c.take<int32_t>((size_t)tc_act_cols(h * 3 * d_h) / 128);
   }
   return w;
 }
@@ -226,6 +235,7 @@ AttnLaunch make_attn(const void* y, int B, int d, int h, int d_h, const void* Wq
   L.q = w.q; L.H = w.H;
   L.rows = w.rows; L.rows_count = w.rows_count; L.need_bits = w.need_bits; L.miss = w.miss;
   L.act_hi = w.act_hi; L.act_lo = w.act_lo;
+  L.tc_part = w.tc_part; L.tc_sem = w.tc_sem;
   return L;
 }
 }  // namespace
@@ -369,6 +379,7 @@ dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, con
   L.idx = idx; L.cap = cap; L.count = count; L.out = out; L.accumulate = accumulate ? 1 : 0;
   L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.bm = w.bm;
   L.act_hi = w.act_hi; L.act_lo = w.act_lo; L.act = w.act; L.ctr = w.ctr;
+  L.tc_part = w.tc_part; L.tc_sem = w.tc_sem;
   cudaError_t e = launch_sparse_mlp(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);
   return e == cudaSuccess ? DV_OK : cuda_fail(e);
 }

@@ -122,6 +122,10 @@ struct MlpLaunch {
   float* act;
   // batch 1: arrival counters of the one-launch MLP (zero between calls)
   int* ctr;
+  // tensor-core path: split-K partial tiles of the up-projection and their
+  // arrival counts (tc_part_floats(min(N, B cap)) floats, one count per tile;
+  // zero between calls)
+  float* tc_part; int* tc_sem;
 };
 
 // Room for the batch union of B lists of up to `cap` neurons out of N.
@@ -133,6 +137,8 @@ int mlp_union_cap(int B, int N, int cap);
 constexpr int kTcMinBatch = 2;
 bool tc_mlp_supported(int B, int d, dv_dtype dt);
 int tc_act_cols(int N);
+// Floats of split-K partial tiles for up to max_rows rows (32 columns a tile).
+size_t tc_part_floats(int max_rows);
 cudaError_t launch_sparse_mlp_tc(const MlpLaunch& a, dv_dtype dt, WsHeader* hdr,
                                  cudaStream_t stream);
 
@@ -150,6 +156,7 @@ struct TcQkvLaunch {
   const uint32_t* member; int words;
   const int32_t* slot_of; const int32_t* pos;
   float* q; void* K; void* V;
+  float* part; int* sem;  // split-K partial tiles (tc_part_floats(max_rows)) and counts, zero between calls
 };
 cudaError_t launch_qkv_tc(const TcQkvLaunch& a, dv_dtype dt, WsHeader* hdr, cudaStream_t stream);
 // out[b] += sum_k coef[b][k] W[rows[k]] with the coefficients split into two
@@ -200,6 +207,7 @@ struct AttnLaunch {
   int32_t* rows; int32_t* rows_count;   // expanded weight rows of the union heads
   uint32_t* need_bits; uint8_t* miss;   // repair plan
   void* act_hi; void* act_lo;           // [32][tc_act_cols(h * d_h)] output-projection coefficients
+  float* tc_part; int* tc_sem;          // q/K/V split-K partial tiles and counts (zero between calls)
 };
 
 

@@ -1242,6 +1242,7 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
     q.max_rows = min(a.h, a.B * a.cap) * per;
     q.member = a.member; q.words = a.hwords; q.slot_of = a.slot_of; q.pos = a.pos;
     q.q = a.q; q.K = a.K; q.V = a.V;
+    q.part = L.tc_part; q.sem = L.tc_sem;
     e = launch_qkv_tc(q, dtype_of<T>(), hdr, stream);
     if (e != cudaSuccess) return e;
   }

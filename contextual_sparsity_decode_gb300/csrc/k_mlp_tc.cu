@@ -6,8 +6,13 @@
 // row's own set as a mask):
 //   up    a[u][b] = ReLU(W^1[:, U[u]] . y_b) * [U[u] in S_b]
 //         M = 128 union neurons per tile, N = B padded to 16/32, K = d,
-//         split over a cluster of S <= 8 CTAs when the union has few tiles
-//         (partials summed through distributed shared memory before ReLU).
+//         split over up to 8 CTAs per tile.  When the largest possible
+//         union has few tiles the host sizes the split: a cluster of S CTAs
+//         per tile, partials summed through distributed shared memory before
+//         ReLU.  Otherwise the split is chosen on the device from the
+//         union's actual size so that the grid (two CTAs per SM) fills the
+//         GPU; those partial tiles are summed with fp32 atomics in L2 and the
+//         tile's last CTA to finish applies the epilogue.
 //         A = gathered rows of W1n (TMA gather4, 128-byte swizzle, K-major),
 //         B = y (TMA tile, K-major).  Accumulator in TMEM; the epilogue writes
 //         a split into two storage-type halves hi + lo (a = hi + lo to ~2^-17
@@ -48,6 +53,8 @@ constexpr int kSD = 4;
 constexpr int kKChunk = 1024;            // union neurons per down-projection CTA, at most
 constexpr long long kUnwindNs = 2000000000LL;  // two seconds
 constexpr uint32_t kTmemCols = 32;
+constexpr int kMaxSplit = 8;             // K splits per up-projection tile, at most
+constexpr int kMinSplitKB = 24;          // K blocks per split, at least
 
 struct UpArgs {
   const int32_t* U;
@@ -69,7 +76,9 @@ struct UpArgs {
   float* q;                 // [B][capQ][d_h]
   void* K;
   void* V;
-  int S;                    // CTAs (one cluster) per tile, splitting K
+  int S;                    // > 1: CTAs (one cluster) per tile, splitting K; 1: split on the device
+  float* part;              // S == 1: [tiles][BP][kTM] fp32 partial tiles, zero between calls
+  int* sem;                 // S == 1: [tiles] arrival counts, zero between calls
 };
 
 // Epilogues of the up kernel: the MLP's masked ReLU split into two storage
@@ -96,9 +105,12 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // thread copies eight 16-byte chunks of the stage into the 128-byte-swizzled
 // K-major layout (16-byte chunk c of row r at chunk c ^ (r % 8) of the row's
 // 128 bytes, rows grouped by 8 in 1024-byte atoms), waits for its copies
-// S - 1 stages later, makes them visible to the async proxy and arrives on
-// the stage's barrier (count 128).  TMA gather4 moves 512 bytes an
-// instruction, which capped a CTA at ~13 GB/s on GB300.
+// S - 2 stages later, makes them visible to the async proxy and arrives on
+// the stage's barrier (count 128).  Signalling S - 2 rather than S - 1
+// stages back leaves the MMA of the oldest stage a stage period before its
+// slot is refilled (measured on GB300: batch-32 OPT-30B-shaped MLP call 154
+// -> 135 us).  TMA gather4 moves 512 bytes an instruction, which capped a
+// CTA at ~13 GB/s on GB300.
 // warps 0-3: loaders + epilogue; warp 4: TMA producer; warp 5: MMA issuer (the
 // two single-thread roles in one warp serialised their waits: 90 against 57 us)
 constexpr int kTcThreads = 192;
@@ -146,10 +158,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long unwind_ns = a.wait_ns > kUnwindNs ? a.wait_ns : kUnwindNs;
   const int cnt = max(0, min(*a.U_count, a.capU));
+  const int nk_all = a.d / kKB;
+  // K splits per tile from the union's actual size (known only here): as
+  // many as the grid holds, at most kMaxSplit, at least kMinSplitKB K blocks
+  // each (shorter slices spend more on the pipeline's fill and the epilogue
+  // than the extra CTAs gain)
   const int S = a.S;
-  const int tile = (int)blockIdx.x / S, split = (int)blockIdx.x % S;
+  const int tiles = (cnt + kTM - 1) / kTM;
+  const int ks = S > 1 ? S
+                       : max(1, min(tiles > 0 ? (int)gridDim.x / tiles : 1, min(kMaxSplit, nk_all / kMinSplitKB)));
+  const int tile = (int)blockIdx.x / ks, split = (int)blockIdx.x % ks;
+  // before any barrier or TMEM use (with S > 1 the whole cluster shares the tile)
+  if (tile >= tiles) return;
   const int u0 = tile * kTM;
-  if (u0 >= cnt) return;  // whole cluster, before any barrier or TMEM use
 
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
@@ -178,9 +199,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const int nk_all = a.d / kKB;
-  const int kb0 = split * nk_all / S;  // this CTA's K blocks [kb0, kb0 + nk)
-  const int nk = (split + 1) * nk_all / S - kb0;
+  const int kb0 = split * nk_all / ks;  // this CTA's K blocks [kb0, kb0 + nk)
+  const int nk = (split + 1) * nk_all / ks - kb0;
 
   if (warp >= 4) {
     if (warp == 4 && lane == 0) {  // TMA producer: y (and the weight rows when they form one tile)
@@ -294,12 +314,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   };
-  if (S == 1) {
+  if (ks == 1) {
     if (tid < kTM) {
 #pragma unroll
       for (int b = 0; b < BP; ++b) emit(tid, b, v[b]);
     }
-  } else {
+  } else if (S > 1) {
     // park the partial tile in the (now idle) ring, then sum rows
     // [split * span, +span) over the cluster's partials
     float* red = reinterpret_cast<float*>(sA);  // [128][BP + 1]
@@ -318,6 +338,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     cluster_arrive();  // no CTA leaves while another reads its partials
     cluster_wait();
+  } else {
+    // add the partial tile into part[tile] (fp32 atomics, performed in L2);
+    // the last of the tile's ks CTAs to arrive applies the epilogue to the
+    // sum and clears part[tile] and the count for the next call
+    __shared__ int last_s;
+    float* pt = a.part + (size_t)tile * BP * kTM;
+    if (tid < kTM && good) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b) atomicAdd(pt + b * kTM + tid, v[b]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last_s = atomicAdd(a.sem + tile, 1) == ks - 1;
+    __syncthreads();
+    if (last_s) {
+      __threadfence();
+      if (tid < kTM) {
+#pragma unroll
+        for (int b = 0; b < BP; ++b) {
+          const float z = __ldcg(pt + b * kTM + tid);
+          pt[b * kTM + tid] = 0.f;
+          emit(tid, b, z);
+        }
+      }
+      if (tid == 0) a.sem[tile] = 0;
+    }
   }
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -491,14 +537,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ---- host ------------------------------------------------------------------------
 
-// CTAs per up-projection tile: double while two CTAs per SM still hold the
-// grid and every slice of d keeps 4+ stages (a small union otherwise leaves
-// most SMs idle: 23 tiles of 128 rows streamed 1.8 MB each).
+// K split of the up-projection (a small union otherwise leaves most SMs
+// idle: 23 tiles of 128 rows streamed 1.8 MB each).  When even the largest
+// possible union has at most half as many tiles as SMs, the host fixes the
+// split: clusters of S CTAs per tile, S doubling while every CTA keeps an SM
+// to itself and a slice of d has 8+ stages.  Otherwise (S = 1) the grid is
+// two CTAs per SM, or one per tile of the largest union when that is more,
+// and each CTA finds its tile and split from the union's actual size on the
+// device (measured on GB300, OPT-30B-shaped batch 32 at 5 %: q/K/V and MLP
+// calls 145 -> 137 and 135 -> 126 us; for batch 4 the host-sized clusters
+// stayed faster, 63 + 53 against 71 + 59 us).
 int up_splits(int tiles, int nk_all) {
   int S = 1;
   while (S < 8 && tiles * S * 2 <= 2 * num_sms_current() && nk_all >= 8 * S) S *= 2;
   return S;
 }
+int up_grid(int max_tiles, int S) { return S > 1 ? max_tiles * S : max(max_tiles, 2 * num_sms_current()); }
 
 // Union entries per down-projection CTA: about two CTAs per SM over the
 // column tiles, 256..1024 entries.
@@ -532,11 +586,13 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   const int maxU = L.N < L.B * L.cap ? L.N : L.B * L.cap;
   UpArgs ua{L.U, L.U_count, L.N, L.member, (L.N + 31) / 32, L.B, L.d, L.N, Upad, L.act_hi, L.act_lo, hdr,
             wait_limit_ns()};
+  ua.part = L.tc_part;
+  ua.sem = L.tc_sem;
   const int tiles = (maxU + kTM - 1) / kTM;
   ua.S = up_splits(tiles, L.d / kKB);
   // neuron rows are gathered by the CTAs' own threads (mapT is not used)
-  cudaError_t e = launch_k(mlp_tc_up_kernel<T, BP, kEpiMlp>, dim3(tiles * ua.S), dim3(kTcThreads), smem_up, stream,
-                           false, ua.S, mY, mY, L.W1n, ua);
+  cudaError_t e = launch_k(mlp_tc_up_kernel<T, BP, kEpiMlp>, dim3(up_grid(tiles, ua.S)), dim3(kTcThreads),
+                           smem_up, stream, false, ua.S, mY, mY, L.W1n, ua);
   if (e != cudaSuccess) return e;
   DownArgs da{L.U, L.U_count, L.N, L.B, L.d, L.N, L.out, hdr, wait_limit_ns()};
   da.kchunk = down_chunk(L.d / kTM, maxU);
@@ -569,10 +625,12 @@ cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream)
   // a head's 3 d_h rows are contiguous: with d_h = 128 every 128-row tile is
   // one head's Q, K or V block
   ua.tile_rows = (3 * L.d_h) % kTM == 0 ? 1 : 0;
+  ua.part = L.part;
+  ua.sem = L.sem;
   const int tiles = (L.max_rows + kTM - 1) / kTM;
   ua.S = up_splits(tiles, L.d / kKB);
-  return launch_k(mlp_tc_up_kernel<T, BP, kEpiQkv>, dim3(tiles * ua.S), dim3(kTcThreads), smem_up, stream, false,
-                  ua.S, mY, mT, L.Wqkv, ua);
+  return launch_k(mlp_tc_up_kernel<T, BP, kEpiQkv>, dim3(up_grid(tiles, ua.S)), dim3(kTcThreads), smem_up,
+                  stream, false, ua.S, mY, mT, L.Wqkv, ua);
 }
 
 template <typename T, int BP>
@@ -620,6 +678,8 @@ bool tc_mlp_supported(int B, int d, dv_dtype dt) {
 }
 
 int tc_act_cols(int N) { return (N + kTM - 1) / kTM * kTM; }
+
+size_t tc_part_floats(int max_rows) { return (size_t)((max_rows + kTM - 1) / kTM) * 32 * kTM; }
 
 cudaError_t launch_sparse_mlp_tc(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, cudaStream_t stream) {
   if (dt == DV_F16) return L.B <= 16 ? run_tc<__half, 16>(L, hdr, stream) : run_tc<__half, 32>(L, hdr, stream);
