@@ -89,7 +89,6 @@ struct MlpWs {
   int32_t* U;
   int32_t* U_count;
   uint32_t* member;
-  uint32_t* bm;
   uint16_t* act_hi;
   uint16_t* act_lo;
   float* act;
@@ -103,7 +102,6 @@ MlpWs carve_mlp(Carver& c, int B, int N, int cap) {
   w.U = c.take<int32_t>((size_t)N);
   w.U_count = c.take<int32_t>(4);
   w.member = c.take<uint32_t>((size_t)B * ((N + 31) / 32));
-  if (B > 1) w.bm = c.take<uint32_t>((size_t)(N + 31) / 32);
   if (B == 1) w.ctr = c.take<int32_t>(8);
   if (B >= kTcMinBatch) {
     w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(N));
@@ -377,7 +375,7 @@ dv_status dv_sparse_mlp(const void* y, int B, int d, int N, const void* W1n, con
   MlpLaunch L{};
   L.y = y; L.B = B; L.d = d; L.N = N; L.W1n = W1n; L.W2n = W2n;
   L.idx = idx; L.cap = cap; L.count = count; L.out = out; L.accumulate = accumulate ? 1 : 0;
-  L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.bm = w.bm;
+  L.U = w.U; L.U_count = w.U_count; L.member = w.member;
   L.act_hi = w.act_hi; L.act_lo = w.act_lo; L.act = w.act; L.ctr = w.ctr;
   L.tc_part = w.tc_part; L.tc_sem = w.tc_sem;
   cudaError_t e = launch_sparse_mlp(L, dt, static_cast<WsHeader*>(ws), num_sms_current(), stream);

@@ -114,7 +114,6 @@ struct MlpLaunch {
   float* out; int accumulate;
   // batch union scratch (B > 1)
   int32_t* U; int32_t* U_count; uint32_t* member;  // member [B][ceil(N/32)]
-  uint32_t* bm;                                     // [ceil(N/32)]: union bitmap of large batches
   // tensor-core path: activations split into two storage-type halves,
   // [32][tc_act_cols(N)] each
   void* act_hi; void* act_lo;
@@ -187,7 +186,7 @@ cudaError_t launch_mlp_stream(const void* y, int d, int N, const void* W1n, cons
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B,
                          int N, int32_t* U, int32_t* U_count, uint32_t* member,
                          int32_t* slot_of, WsHeader* hdr, cudaStream_t stream,
-                         uint32_t* clear = nullptr, uint32_t* bm_global = nullptr);
+                         uint32_t* clear = nullptr);
 
 // ---- attention (k_attn.cu) ---------------------------------------------------
 

@@ -255,42 +255,58 @@ __global__ void __launch_bounds__(1024) union_kernel(const int32_t* idx, int cap
 }
 
 
-// Large unions (many rows x long lists) in two passes: every entry marks
-// the union bitmap and its row's membership bitmap in global memory (both
-// zeroed before), spread over a grid; then one CTA lists the union.
-__global__ void __launch_bounds__(256) union_mark_kernel(const int32_t* idx, int cap, const int32_t* count, int N,
-                                                         uint32_t* bm, uint32_t* member, WsHeader* hdr) {
-  const int b = blockIdx.y, e = blockIdx.x * 256 + threadIdx.x;
+// Large unions (many rows x long lists) in two passes.  One CTA per row
+// builds the row's membership bitmap in shared memory from its list and
+// writes it out whole (no global atomics, nothing to clear first); then one
+// CTA ORs the rows' bitmaps word by word and lists the union.  (The version
+// that marked every entry with two global atomicOr took 30 + 18 us for 32
+// rows of 14336 entries.)
+__global__ void __launch_bounds__(1024) union_rows_kernel(const int32_t* idx, int cap, const int32_t* count, int N,
+                                                          uint32_t* member, WsHeader* hdr) {
+  extern __shared__ uint32_t bm[];
+  const int b = blockIdx.x;
   const int words = (N + 31) / 32;
+  for (int i = threadIdx.x; i < words; i += blockDim.x) bm[i] = 0u;
   int cnt = count[b];
   if (cnt > cap) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(hdr, DV_ERR_CAPACITY, cnt);
+    if (threadIdx.x == 0) set_error(hdr, DV_ERR_CAPACITY, cnt);
     cnt = cap;
   }
-  if (e >= cnt) return;
-  const int j = idx[(size_t)b * cap + e];
-  if (j < 0 || j >= N) {
-    set_error(hdr, DV_ERR_INDEX_RANGE, j);
-    return;
+  cnt = max(cnt, 0);
+  __syncthreads();
+  const int32_t* row = idx + (size_t)b * cap;
+  for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+    const int j = row[e];
+    if (j < 0 || j >= N) {
+      set_error(hdr, DV_ERR_INDEX_RANGE, j);
+      continue;
+    }
+    atomicOr(&bm[j >> 5], 1u << (j & 31));
   }
-  const uint32_t bit = 1u << (j & 31);
-  atomicOr(bm + (j >> 5), bit);
-  atomicOr(member + (size_t)b * words + (j >> 5), bit);
+  __syncthreads();
+  for (int i = threadIdx.x; i < words; i += blockDim.x) member[(size_t)b * words + i] = bm[i];
 }
 
-__global__ void __launch_bounds__(1024) union_list_kernel(const uint32_t* bm, int N, int32_t* U, int32_t* U_count,
-                                                          int32_t* slot_of) {
+__device__ __forceinline__ uint32_t union_word(const uint32_t* member, int B, int words, int i) {
+  uint32_t m = 0u;
+#pragma unroll 8
+  for (int b = 0; b < B; ++b) m |= __ldcg(member + (size_t)b * words + i);
+  return m;
+}
+
+__global__ void __launch_bounds__(1024) union_list_kernel(const uint32_t* member, int B, int N, int32_t* U,
+                                                          int32_t* U_count, int32_t* slot_of) {
   __shared__ int tmp[32];
   const int words = (N + 31) / 32;
   const int WW = (words + 1023) / 1024;
   const int w0 = min(words, (int)threadIdx.x * WW), w1 = min(words, w0 + WW);
   int mine = 0;
-  for (int i = w0; i < w1; ++i) mine += __popc(bm[i]);
+  for (int i = w0; i < w1; ++i) mine += __popc(union_word(member, B, words, i));
   int total;
   const int incl = block_inclusive_scan<1024>(mine, tmp, &total);
   int o = incl - mine;
   for (int i = w0; i < w1; ++i) {
-    uint32_t m = bm[i];
+    uint32_t m = union_word(member, B, words, i);
     while (m) {
       const int bit = __ffs(m) - 1;
       if (slot_of) slot_of[i * 32 + bit] = o;
@@ -403,16 +419,13 @@ int mlp_union_cap(int B, int N, int cap) {
 
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B, int N,
                          int32_t* U, int32_t* U_count, uint32_t* member, int32_t* slot_of,
-                         WsHeader* hdr, cudaStream_t stream, uint32_t* clear, uint32_t* bm_global) {
+                         WsHeader* hdr, cudaStream_t stream, uint32_t* clear) {
   const size_t words = (size_t)((N + 31) / 32);
-  if (bm_global && (long long)B * cap > 8192 && !clear) {  // two passes over a grid
-    cudaError_t e = cudaMemsetAsync(bm_global, 0, words * sizeof(uint32_t), stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(member, 0, (size_t)B * words * sizeof(uint32_t), stream);
+  if ((long long)B * cap > 8192 && !clear) {  // two passes: a CTA per row, then the list
+    union_rows_kernel<<<B, 1024, words * sizeof(uint32_t), stream>>>(idx, cap, count, N, member, hdr);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    union_mark_kernel<<<dim3((cap + 255) / 256, B), 256, 0, stream>>>(idx, cap, count, N, bm_global, member, hdr);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    union_list_kernel<<<1, 1024, 0, stream>>>(bm_global, N, U, U_count, slot_of);
+    union_list_kernel<<<1, 1024, 0, stream>>>(member, B, N, U, U_count, slot_of);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(2);
     return e;
@@ -433,8 +446,7 @@ cudaError_t launch_sparse_mlp(const MlpLaunch& L, dv_dtype dt, WsHeader* hdr, in
     if (e != cudaSuccess) return e;
   }
   if (L.B > 1) {
-    e = launch_union(L.idx, L.cap, L.count, L.B, L.N, L.U, L.U_count, L.member, nullptr, hdr,
-                     stream, nullptr, L.bm);
+    e = launch_union(L.idx, L.cap, L.count, L.B, L.N, L.U, L.U_count, L.member, nullptr, hdr, stream);
     if (e != cudaSuccess) return e;
   }
   if (tc) return launch_sparse_mlp_tc(L, dt, hdr, stream);
