@@ -122,6 +122,8 @@ struct AttnWs {
   float* H;
   int32_t* rows;
   int32_t* rows_count;
+  int32_t* rows_o;
+  int32_t* rows_o_count;
   uint32_t* need_bits;
   uint8_t* miss;
   uint16_t* act_hi;
@@ -141,6 +143,8 @@ AttnWs carve_attn(Carver& c, int B, int h, int d_h, int cap, int n_max) {
   if (B >= kTcMinBatch) {  // tensor-core path (16-bit types)
     w.rows = c.take<int32_t>((size_t)h * 3 * d_h);
     w.rows_count = c.take<int32_t>(4);
+    w.rows_o = c.take<int32_t>((size_t)h * d_h);
+    w.rows_o_count = c.take<int32_t>(4);
     w.need_bits = c.take<uint32_t>((size_t)(h + 31) / 32);
     w.miss = c.take<uint8_t>((size_t)B * h);
     w.act_hi = c.take<uint16_t>((size_t)32 * tc_act_cols(h * d_h));
@@ -232,6 +236,7 @@ AttnLaunch make_attn(const void* y, int B, int d, int h, int d_h, const void* Wq
   L.U = w.U; L.U_count = w.U_count; L.member = w.member; L.slot_of = w.slot_of;
   L.q = w.q; L.H = w.H;
   L.rows = w.rows; L.rows_count = w.rows_count; L.need_bits = w.need_bits; L.miss = w.miss;
+  L.rows_o = w.rows_o; L.rows_o_count = w.rows_o_count;
   L.act_hi = w.act_hi; L.act_lo = w.act_lo;
   L.tc_part = w.tc_part; L.tc_sem = w.tc_sem;
   return L;

@@ -181,12 +181,22 @@ cudaError_t launch_mlp_stream(const void* y, int d, int N, const void* W1n, cons
                               const int32_t* list, const int32_t* count, int cap, dv_dtype dt, float* out,
                               WsHeader* hdr, int num_sms, int pdl, cudaStream_t stream);
 
+// Weight-row lists of the union's units, written by the union kernel: for
+// list q (rows[q] non-null), rows[q][k] = U[k / per[q]] * per[q] + k % per[q]
+// for every unit of U, and count[q] = |U| per[q] (the attention's tensor-core
+// projections: per = 3 d_h Wqkv rows and d_h W^O rows per head).
+struct RowsExpand {
+  int32_t* rows[2];
+  int32_t* count[2];
+  int per[2];
+};
 // Union of per-row index lists: U ascending, U_count, member bitmaps and
-// (optional) slot_of[unit] = position of the unit in U.
+// (optional) slot_of[unit] = position of the unit in U; with `ex`, also its
+// row lists (single-CTA path only, i.e. with `clear`).
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B,
                          int N, int32_t* U, int32_t* U_count, uint32_t* member,
                          int32_t* slot_of, WsHeader* hdr, cudaStream_t stream,
-                         uint32_t* clear = nullptr);
+                         uint32_t* clear = nullptr, const RowsExpand* ex = nullptr);
 
 // ---- attention (k_attn.cu) ---------------------------------------------------
 
@@ -203,7 +213,8 @@ struct AttnLaunch {
   float* q;                   // [B][capU][d_h]
   float* H;                   // [B][capU][d_h]
   // batches on the tensor-core path (B >= kTcMinBatch), else null
-  int32_t* rows; int32_t* rows_count;   // expanded weight rows of the union heads
+  int32_t* rows; int32_t* rows_count;   // expanded Wqkv rows of the union heads
+  int32_t* rows_o; int32_t* rows_o_count;  // expanded W^O rows of the union heads
   uint32_t* need_bits; uint8_t* miss;   // repair plan
   void* act_hi; void* act_lo;           // [32][tc_act_cols(h * d_h)] output-projection coefficients
   float* tc_part; int* tc_sem;          // q/K/V split-K partial tiles and counts (zero between calls)

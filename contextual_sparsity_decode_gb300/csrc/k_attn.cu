@@ -619,19 +619,6 @@ __global__ void __launch_bounds__(256) repair_plan_kernel(AttnArgs a, uint32_t* 
   }
 }
 
-// rows[k] = U[k / per] * per + k % per for the per rows of every union head
-// (per = 3 d_h: its Wqkv rows; per = d_h: its W^O rows), and their count.
-__global__ void expand_rows_kernel(const int32_t* U, const int32_t* U_count, int h, int per, int32_t* rows,
-                                   int32_t* rows_count) {
-  const int cnt = max(0, min(*U_count, h));
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k == 0) *rows_count = cnt * per;
-  if (k < cnt * per) {
-    const int u = k / per;
-    rows[k] = U[u] * per + (k - u * per);
-  }
-}
-
 // The output projection's coefficients for the tensor cores: H[b][u][t] of
 // the heads row b selected (0 elsewhere, and for the padding rows), split
 // into two storage-type halves hi + lo, laid out [BP][Upad].
@@ -1230,12 +1217,8 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
     e = launch_k(attn_qkv_kernel<T, 4, 2>, dim3(grid), dim3(256), 0, stream, pdl != 0, 1, a, RG, tl, pdl);
   }
   if (e != cudaSuccess) return e;
-  if (tc) {  // the current tokens' q and K/V
+  if (tc) {  // the current tokens' q and K/V (the Wqkv row list comes from the union kernel)
     const int per = 3 * a.d_h;
-    expand_rows_kernel<<<(a.h * per + 255) / 256, 256, 0, stream>>>(a.U, a.U_count, a.h, per, L.rows, L.rows_count);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    count_launches(1);
     TcQkvLaunch q{};
     q.y = L.y; q.B = a.B; q.d = a.d; q.h = a.h; q.d_h = a.d_h; q.n_max = a.n_max; q.capQ = a.capU;
     q.Wqkv = L.Wqkv; q.rows = L.rows; q.rows_count = L.rows_count;
@@ -1249,11 +1232,7 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
   // 2. split-KV softmax, one cluster per (row, head), cache bookkeeping
   e = launch_decode<T>(a, stream);
   if (e != cudaSuccess) return e;
-  if (tc) {  // 3. output projection on the tensor cores
-    expand_rows_kernel<<<(a.h * a.d_h + 255) / 256, 256, 0, stream>>>(a.U, a.U_count, a.h, a.d_h, L.rows,
-                                                                      L.rows_count);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  if (tc) {  // 3. output projection on the tensor cores (the W^O row list comes from the union kernel)
     const int Upad = tc_act_cols(a.h * a.d_h);
     const int BP = a.B <= 16 ? 16 : 32;
     coef_split_kernel<T><<<dim3((Upad + 255) / 256, BP), 256, 0, stream>>>(
@@ -1268,7 +1247,7 @@ cudaError_t attn_t(const AttnLaunch& L, WsHeader* hdr, int num_sms, cudaStream_t
     }
     TcRowsLaunch r{};
     r.W = L.Wo; r.n_rows = a.h * a.d_h; r.d = a.d; r.B = a.B; r.rows_per_unit = a.d_h;
-    r.rows = L.rows; r.rows_count = L.rows_count; r.max_rows = min(a.h, a.B * a.cap) * a.d_h;
+    r.rows = L.rows_o; r.rows_count = L.rows_o_count; r.max_rows = min(a.h, a.B * a.cap) * a.d_h;
     r.act_hi = L.act_hi; r.act_lo = L.act_lo; r.Upad = Upad; r.out = L.out;
     return launch_rows_tc(r, dtype_of<T>(), hdr, stream);
   }
@@ -1310,8 +1289,13 @@ cudaError_t repair_t(const AttnLaunch& L, WsHeader* hdr, cudaStream_t stream) {
 cudaError_t launch_sparse_attn(const AttnLaunch& L, dv_dtype dt, WsHeader* hdr, int num_sms,
                                cudaStream_t stream) {
   if (L.B > 1) {
+    RowsExpand ex{};
+    if (L.rows && L.rows_o) {  // row lists of the tensor-core projections
+      ex.rows[0] = L.rows; ex.count[0] = L.rows_count; ex.per[0] = 3 * L.d_h;
+      ex.rows[1] = L.rows_o; ex.count[1] = L.rows_o_count; ex.per[1] = L.d_h;
+    }
     cudaError_t e = launch_union(L.head_idx, L.cap, L.head_count, L.B, L.h, L.U, L.U_count,
-                                 L.member, L.slot_of, hdr, stream, L.need_bits);
+                                 L.member, L.slot_of, hdr, stream, L.need_bits, &ex);
     if (e != cudaSuccess) return e;
   }
   switch (dt) {

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(1024) union_kernel(const int32_t* idx, int cap, const int32_t* count,
                                                      int B, int N, int32_t* U, int32_t* U_count,
                                                      uint32_t* member, int32_t* slot_of,
-                                                     WsHeader* hdr, uint32_t* clear) {
+                                                     WsHeader* hdr, uint32_t* clear, RowsExpand ex) {
   extern __shared__ uint32_t bm[];
   __shared__ int tmp[32];
   const int words = (N + 31) / 32;
@@ -252,6 +252,18 @@ __global__ void __launch_bounds__(1024) union_kernel(const int32_t* idx, int cap
     }
   }
   if (threadIdx.x == 0) *U_count = total;
+  // the row lists of the union's units (U as written above by this CTA)
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    if (!ex.rows[q]) continue;
+    const int per = ex.per[q];
+    if (threadIdx.x == 0) *ex.count[q] = total * per;
+    for (int k = threadIdx.x; k < total * per; k += blockDim.x) {
+      const int u = k / per;
+      ex.rows[q][k] = U[u] * per + (k - u * per);
+    }
+  }
 }
 
 
@@ -419,7 +431,7 @@ int mlp_union_cap(int B, int N, int cap) {
 
 cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int B, int N,
                          int32_t* U, int32_t* U_count, uint32_t* member, int32_t* slot_of,
-                         WsHeader* hdr, cudaStream_t stream, uint32_t* clear) {
+                         WsHeader* hdr, cudaStream_t stream, uint32_t* clear, const RowsExpand* ex) {
   const size_t words = (size_t)((N + 31) / 32);
   if ((long long)B * cap > 8192 && !clear) {  // two passes: a CTA per row, then the list
     union_rows_kernel<<<B, 1024, words * sizeof(uint32_t), stream>>>(idx, cap, count, N, member, hdr);
@@ -431,7 +443,9 @@ cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int 
     return e;
   }
   const size_t smem = words * sizeof(uint32_t);
-  union_kernel<<<1, 1024, smem, stream>>>(idx, cap, count, B, N, U, U_count, member, slot_of, hdr, clear);
+  const RowsExpand none{};
+  union_kernel<<<1, 1024, smem, stream>>>(idx, cap, count, B, N, U, U_count, member, slot_of, hdr, clear,
+                                          ex ? *ex : none);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(1);
   return e;
