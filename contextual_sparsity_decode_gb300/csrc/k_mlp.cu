@@ -299,10 +299,17 @@ __global__ void __launch_bounds__(1024) union_rows_kernel(const int32_t* idx, in
   for (int i = threadIdx.x; i < words; i += blockDim.x) member[(size_t)b * words + i] = bm[i];
 }
 
+constexpr int kUnionMaxB = 32;      // rows of a batch, at most
+constexpr int kUnionMaxWW = 2;      // words per thread: N <= 65536 is 2048 words over 1024 threads
+
+// OR of word i over the B rows' bitmaps: every row's load is issued at once
 __device__ __forceinline__ uint32_t union_word(const uint32_t* member, int B, int words, int i) {
+  uint32_t v[kUnionMaxB];
+#pragma unroll
+  for (int b = 0; b < kUnionMaxB; ++b) v[b] = b < B ? __ldcg(member + (size_t)b * words + i) : 0u;
   uint32_t m = 0u;
-#pragma unroll 8
-  for (int b = 0; b < B; ++b) m |= __ldcg(member + (size_t)b * words + i);
+#pragma unroll
+  for (int b = 0; b < kUnionMaxB; ++b) m |= v[b];
   return m;
 }
 
@@ -310,15 +317,22 @@ __global__ void __launch_bounds__(1024) union_list_kernel(const uint32_t* member
                                                           int32_t* U_count, int32_t* slot_of) {
   __shared__ int tmp[32];
   const int words = (N + 31) / 32;
-  const int WW = (words + 1023) / 1024;
+  const int WW = (words + 1023) / 1024;  // <= kUnionMaxWW
   const int w0 = min(words, (int)threadIdx.x * WW), w1 = min(words, w0 + WW);
+  uint32_t mw[kUnionMaxWW];
   int mine = 0;
-  for (int i = w0; i < w1; ++i) mine += __popc(union_word(member, B, words, i));
+#pragma unroll
+  for (int q = 0; q < kUnionMaxWW; ++q) {
+    mw[q] = w0 + q < w1 ? union_word(member, B, words, w0 + q) : 0u;
+    mine += __popc(mw[q]);
+  }
   int total;
   const int incl = block_inclusive_scan<1024>(mine, tmp, &total);
   int o = incl - mine;
-  for (int i = w0; i < w1; ++i) {
-    uint32_t m = union_word(member, B, words, i);
+#pragma unroll
+  for (int q = 0; q < kUnionMaxWW; ++q) {
+    const int i = w0 + q;
+    uint32_t m = mw[q];
     while (m) {
       const int bit = __ffs(m) - 1;
       if (slot_of) slot_of[i * 32 + bit] = o;
