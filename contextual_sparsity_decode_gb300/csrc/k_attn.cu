@@ -1101,23 +1101,27 @@ bool decode_width_fits(int w) {
 }
 
 // With many (row, head) pairs the GPU is full anyway, and wider clusters
-// only add cluster barriers and co-scheduling constraints: from 64 pairs on
-// the cluster is 8 CTAs wide, from 256 pairs 4 (each warp then takes
-// several batches of positions).  Measured at OPT-30B width, 2048
-// positions, 32 rows: 896 pairs 309 us (8 wide) and 487 us (16 wide) for
-// 941 MB, the whole attention call 528 us at 4 wide against 591 at 8.
-// DV_DECODE_WIDTH in the environment forces a width (4..16).
+// only add cluster barriers, co-scheduling constraints and partial sums to
+// combine: from 32 pairs on the cluster is 4 CTAs wide, from 64 pairs 2,
+// from 640 pairs one CTA per pair (each warp then takes several batches of
+// positions).  Measured on GB300 at OPT-30B width, ~2050 positions, whole
+// layers: 896 pairs 555 / 528 / 521 us per layer at 4 / 2 / 1 wide; 448
+// pairs 417 / 399 / 411 at 4 / 2 / 1; 96-112 pairs 275 / 271 and 313 / 302
+// at 8 / 2 (1 wide: 286, 316); 48 pairs 211 / 201 / 208 at 16 / 4 / 2; 12
+// pairs 121 / 120 / 124 at 16 / 8 / 4.
+// DV_DECODE_WIDTH in the environment forces a width (1..16).
 template <typename T, int DH>
 int decode_cluster_width(int n_max, int pairs) {
   static const int forced = [] {
     const char* e = getenv("DV_DECODE_WIDTH");
     return e ? atoi(e) : 0;
   }();
-  if (forced >= 4 && forced <= kMaxCSd && decode_width_fits<T, DH>(forced)) return forced;
+  if (forced >= 1 && forced <= kMaxCSd && decode_width_fits<T, DH>(forced)) return forced;
   constexpr int kPos = kDecWarps * 16;  // positions per CTA in one batch (kPW = 16)
   int want = min(kMaxCSd, max(8, (n_max + kPos - 1) / kPos));
-  if (pairs >= 64) want = 8;
-  if (pairs >= 256) want = 4;
+  if (pairs >= 32) want = 4;
+  if (pairs >= 64) want = 2;
+  if (pairs >= 640) want = 1;
   if (decode_width_fits<T, DH>(want)) return want;
   return decode_width_fits<T, DH>(8) ? 8 : 4;
 }
