@@ -52,6 +52,11 @@ CASES = [
     ("batch16_f16_tc",   16, 512, 8,  64,  "f16",  [20 + b for b in range(16)], 64, 6, 3, "isq", None),
     ("batch32_bf16_tc",  32, 256, 8,  128, "bf16", [9 + (7 * b) % 23 for b in range(32)], 48, 5, "rnd",
      "one", None),
+    # 32 rows x 20 heads = 640 (row, head) pairs: one decode CTA per pair (no split over a cluster)
+    ("pairs640_f16_dh64",   32, 256, 24, 64,  "f16",  [10 + (5 * b) % 17 for b in range(32)], 48, 3, 20,
+     "isq", None),
+    ("pairs640_bf16_dh128", 32, 256, 24, 128, "bf16", [7 + (3 * b) % 19 for b in range(32)], 32, 3, 20,
+     "isq", None),
 ]
 
 
