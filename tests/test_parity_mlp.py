@@ -52,7 +52,7 @@ def _sets(name, B, N, k):
     return [torch.sort(torch.randperm(N, generator=g)[:k]).values.to(torch.int32) for _ in range(B)]
 
 
-def _run(y, W1n, W2n, sets, cap, accumulate=False, base=None):
+def _run(y, W1n, W2n, sets, cap, accumulate=False, base=None, ws=None):
     dev = "cuda"
     B, d = y.shape
     idx = torch.full((B, cap), -1, dtype=torch.int32)
@@ -61,7 +61,8 @@ def _run(y, W1n, W2n, sets, cap, accumulate=False, base=None):
         idx[b, : len(s)] = s
         cnt[b] = len(s)
     out = (base.clone() if base is not None else torch.full((B, d), 123.0)).to(dev)
-    ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(B, d, W1n.shape[0], cap))
+    if ws is None:
+        ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(B, d, W1n.shape[0], cap))
     dv.dv_sparse_mlp(y.to(dev), W1n.to(dev), W2n.to(dev), idx.to(dev), cnt.to(dev), out, ws,
                      accumulate=accumulate)
     st, info = dv.dv_check(ws)
@@ -220,3 +221,55 @@ def test_large_batch_union_with_out_of_range_index():
     ref = oracle.sparse_mlp_batched(f64(y), f64(W1n), f64(W2n), [s[s < N].numpy() for s in sets])
     for b in range(B):
         assert_rel_l2(out[b], ref[b], "f16", f"row {b}")
+
+
+@pytest.mark.tc
+def test_device_split_up_projection_partial_tiles():
+    """32 rows whose sets overlap heavily: the largest possible union (all
+    28672 neurons) has more tiles than half the SMs, so the up-projection's
+    K split is chosen on the device from the actual union (16 or ~80 tiles
+    of 128: 4 or 3 splits, partial tiles summed with fp32 atomics and
+    finished by each tile's last CTA).  Three calls on one workspace, the
+    union shrinking and growing between them, each against the oracle (the
+    partial tiles and their counts must come back to zero after every call)."""
+    B, d, N, k = 32, 7168, 28672, 1434
+    name = "dsplit"
+    W1n, W2n = _weights(name, d, N, "bf16")
+    ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(B, d, N, k))
+    g = torch.Generator().manual_seed(77)
+    for call, pool_n in enumerate((2000, 10000, 2000)):
+        pool = torch.randperm(N, generator=g)[:pool_n]
+        sets = [torch.sort(pool[torch.randperm(pool_n, generator=g)[:k]]).values.to(torch.int32)
+                for _ in range(B)]
+        y = draw((B, d), 1.0, 212, f"{name}/y{call}", "bf16")
+        base = draw((B, d), 1.0, 212, f"{name}/base{call}", "f32")
+        out, st, info = _run(y, W1n, W2n, sets, k, accumulate=True, base=base, ws=ws)
+        assert (st, info) == (0, 0), (call, st, info)
+        ref = oracle.sparse_mlp_batched(f64(y), f64(W1n), f64(W2n), [s.numpy() for s in sets])
+        for b in range(B):
+            assert_rel_l2(out[b] - f64(base)[b], ref[b], "bf16", f"call {call} row {b}")
+
+
+@pytest.mark.parametrize("B,cap", [(4, 100), (16, 600)], ids=["one_cta_union", "two_pass_union"])
+def test_batch_count_above_capacity_is_clamped_and_reported(B, cap):
+    """A row whose count exceeds the list's capacity: the union uses its
+    first cap entries and reports DV_ERR_CAPACITY (the single-CTA union
+    below 8192 entries and the two-pass union above)."""
+    d, N = 1024, 4096
+    name = f"capx_{B}"
+    W1n, W2n = _weights(name, d, N, "f16")
+    y = draw((B, d), 1.0, 213, name + "/y", "f16")
+    sets = _sets(name, B, N, cap)
+    dev = "cuda"
+    idx = torch.stack(sets).to(torch.int32)
+    cnt = torch.full((B,), cap, dtype=torch.int32)
+    cnt[1] = cap + 5
+    out = torch.zeros(B, d, device=dev)
+    ws = dv.workspace(dv.dv_sparse_mlp_workspace_size(B, d, N, cap))
+    dv.dv_sparse_mlp(y.to(dev), W1n.to(dev), W2n.to(dev), idx.to(dev), cnt.to(dev), out, ws)
+    st, info = dv.dv_check(ws)
+    assert (st, info) == (8, cap + 5)  # DV_ERR_CAPACITY
+    ref = oracle.sparse_mlp_batched(f64(y), f64(W1n), f64(W2n), [s.numpy() for s in sets])
+    got = out.cpu().double().numpy()
+    for b in range(B):
+        assert_rel_l2(got[b], ref[b], "f16", f"row {b}")
