@@ -448,6 +448,7 @@ cudaError_t launch_union(const int32_t* idx, int cap, const int32_t* count, int 
                          WsHeader* hdr, cudaStream_t stream, uint32_t* clear, const RowsExpand* ex) {
   const size_t words = (size_t)((N + 31) / 32);
   if ((long long)B * cap > 8192 && !clear) {  // two passes: a CTA per row, then the list
+    if (B > kUnionMaxB || words > (size_t)1024 * kUnionMaxWW) return cudaErrorInvalidValue;
     union_rows_kernel<<<B, 1024, words * sizeof(uint32_t), stream>>>(idx, cap, count, N, member, hdr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -590,6 +590,7 @@ cudaError_t run_tc(const MlpLaunch& L, WsHeader* hdr, cudaStream_t stream) {
   ua.sem = L.tc_sem;
   const int tiles = (maxU + kTM - 1) / kTM;
   ua.S = up_splits(tiles, L.d / kKB);
+  if (ua.S == 1 && (!ua.part || !ua.sem)) return cudaErrorInvalidValue;  // the device split needs them
   // neuron rows are gathered by the CTAs' own threads (mapT is not used)
   cudaError_t e = launch_k(mlp_tc_up_kernel<T, BP, kEpiMlp>, dim3(up_grid(tiles, ua.S)), dim3(kTcThreads),
                            smem_up, stream, false, ua.S, mY, mY, L.W1n, ua);
@@ -629,6 +630,7 @@ cudaError_t run_qkv_tc(const TcQkvLaunch& L, WsHeader* hdr, cudaStream_t stream)
   ua.sem = L.sem;
   const int tiles = (L.max_rows + kTM - 1) / kTM;
   ua.S = up_splits(tiles, L.d / kKB);
+  if (ua.S == 1 && (!ua.part || !ua.sem)) return cudaErrorInvalidValue;  // the device split needs them
   return launch_k(mlp_tc_up_kernel<T, BP, kEpiQkv>, dim3(up_grid(tiles, ua.S)), dim3(kTcThreads), smem_up,
                   stream, false, ua.S, mY, mT, L.Wqkv, ua);
 }
